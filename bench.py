@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP8 linear layer (dynamic activation quantize + block-scaled GEMM).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the layer over the prefill MLP-up workload (x bf16
+[4096, 4096] quantised to MXFP8 in the step, weights E4M3 [14336, 4096] with
+E8M0 block scales, bf16 out [4096, 14336]): the quantize kernel, then the
+tcgen05 GEMM with its bias/bf16 epilogue.  Inputs are resident in HBM; the L2
+is flushed (a 256 MiB write) between timed steps, outside the timed events.
+Prints one JSON line (rank 0).  Secondary figures: the decode sweep (M = 1, 4,
+16, 64; N = K = 4096) as HBM GB/s, and the per-kernel split.
+
+With N > 1 (torchrun) every rank runs the same workload on its own GPU
+(independent replicas: the layer has no exchange step); value is the work of
+all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain fp64 numpy implementation in
+oracle/) on the host cores, on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded; pin numpy's BLAS before it loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mxfp8_block_scaled_02_gb300 import synth  # noqa: E402
+
+METRIC = "MXFP8 linear TFLOP/s (quant+GEMM) and % of GB300 FP8 peak; decode HBM GB/s"
+WORKLOAD = "prefill MLP-up M4096 N14336 K4096, bf16 x quantised in the step, no bias"
+FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_prefill_up.traffic.txt")
+GEMM_SOURCE = os.path.join(ROOT, "mxfp8_block_scaled_02_gb300", "csrc", "gemm.cu")
+
+
+def _dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _traffic_for_current_gemm():
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches gemm.cu."""
+    try:
+        kv = dict(line.split("=", 1) for line in open(TRAFFIC_FILE).read().split() if "=" in line)
+        src_hash = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()[:16]
+        if kv.get("gemm_cu_sha256_16") != src_hash:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def _dev_bf16(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _cpu_oracle_rate(p: synth.LinearProblem, rows: int, cols: int, min_seconds: float):
+    """Oracle quant+GEMM on a rows x cols sample of the output; TFLOP/s and details."""
+    import oracle
+    x = synth.bf16_bits_to_f64(p.x[0, :rows])
+    wq, ws = oracle.quantize(synth.bf16_bits_to_f64(p.w[0, :cols]))   # setup, not timed
+    flops = 2.0 * rows * cols * p.K
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.linear_bf16(x, wq, ws)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return flops * reps / el / 1e12, el, reps
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, bounded samples of the same workload."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return
+    p = synth.prefill_up()
+    import oracle
+    rows, cols = 4, 256
+    x = synth.bf16_bits_to_f64(p.x[0, :rows])
+    wq, ws = oracle.quantize(synth.bf16_bits_to_f64(p.w[0, :cols]))
+    flops = 2.0 * rows * cols * p.K
+    for _ in range(args.warmup):
+        oracle.linear_bf16(x, wq, ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.linear_bf16(x, wq, ws)
+    el = time.perf_counter() - t0
+    value = flops * args.steps / el / 1e12
+    sample = f"{rows} rows x {cols} output columns x K={p.K} of the workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64 generator)",
+        "config": {"workload": WORKLOAD, "M": p.M, "N": p.N, "K": p.K, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    from mxfp8_block_scaled_02_gb300 import build, ops
+    rank, world, local_rank = _dist_env()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build.build()
+    ops.load()
+
+    p = synth.prefill_up()
+    M, N, K = p.M, p.N, p.K
+    flops = p.flops
+    x = _dev_bf16(p.x[0], dev)
+    w = _dev_bf16(p.w[0], dev)
+    wq, ws = ops.quantize(w)                    # weights quantised once (E4M3 + E8M0)
+    pw = ops.process_weights(wq, ws)
+    del w, wq, ws
+    x_q = torch.empty((1, M, K), dtype=torch.uint8, device=dev)
+    sfa = torch.empty(ops.packed_sizes(1, M, K)[1], dtype=torch.uint8, device=dev)
+    out = torch.empty((1, M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa = ops.quantize_packed(x, 1, x_q=x_q, sf_packed=sfa)
+        ops.gemm_packed(pa, pw, out=out)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    ops.check()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c]
+    clocks = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else str(local_rank))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(n):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        pa = ops.quantize_packed(x, 1, x_q=x_q, sf_packed=sfa)
+        e1.record(stream)
+        ops.gemm_packed(pa, pw, out=out)
+        e2.record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ops.check()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(n)]
+    q_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    g_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / n
+    value = flops * world * n / (total_ms * 1e-3) / 1e12
+
+    gemm_ms = statistics.mean(g_ms)
+    quant_ms = statistics.mean(q_ms)
+    peaks, peak_src = _peaks()
+    fp8_peak = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) * FP8_PER_BF16
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    traffic = _traffic_for_current_gemm()
+    quant_bytes = M * K * 2 + M * K + M * K // 32
+
+    # single-call public API (the same two kernels behind one C-ABI call)
+    ws = torch.empty(ops.workspace_size(1, M, N, K, False), dtype=torch.uint8, device=dev)
+    lin_ms = []
+    for i in range(min(n, 200)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ops.linear(x, pw, out=out[0], workspace=ws)
+        b.record(stream)
+        flush.zero_()
+        lin_ms.append((a, b))
+    torch.cuda.synchronize()
+    lin_ms = statistics.mean(a.elapsed_time(b) for a, b in lin_ms)
+
+    # end to end through the public call with host buffers
+    x_host = torch.from_numpy(p.x[0].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_steps = max(3, min(n, 50))
+    for i in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        ops.linear(x_dev, pw, out=out[0], workspace=ws)
+        out_host.copy_(out[0], non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        ops.linear(x_dev, pw, out=out[0], workspace=ws)
+        out_host.copy_(out[0], non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    ops.check()
+
+    decode = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 500))
+
+    line = None
+    if rank == 0:
+        cpu_rate, cpu_s, cpu_reps = _cpu_oracle_rate(p, rows=16, cols=1024, min_seconds=10.0)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 x e4m3 -> fp32 accumulate (MXFP8, E8M0 block scales), bf16 out",
+            "data": "synthetic (seeded SplitMix64 generator; random-init weights)",
+            "config": {"workload": WORKLOAD, "B": 1, "M": M, "N": N, "K": K,
+                       "x": "bf16 N(0,1), 0.1% entries x100, 1% of 32-blocks zero",
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "parallelism": f"replicas x{world}"},
+            "fp8_peak_fraction": value / fp8_peak,
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": traffic,
+                         "kernel": "gemm_mxf8_kernel (tcgen05 kind::mxf8f6f4 block_scale)",
+                         "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16:g} (nominal FP8/BF16)"},
+            "kernels": {"quantize_us": quant_ms * 1e3,
+                        "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9,
+                        "quantize_hbm_frac": quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm_peak,
+                        "gemm_us": gemm_ms * 1e3, "gemm_tflops": gemm_tflops,
+                        "linear_call_us": lin_ms * 1e3},
+            "decode_hbm": decode,
+            "cpu_baseline": {"value": cpu_rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": f"16 rows x 1024 output columns x K={K}, "
+                                       f"{cpu_reps} calls in {cpu_s:.1f} s (fp64 numpy, 1 thread)"},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * n,
+            "clocks": clk,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def _decode_sweep(ops, dev, flush, stream, steps):
+    """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the whole layer."""
+    p = synth.decode(64)
+    w = _dev_bf16(p.w[0], dev)
+    wq, ws = ops.quantize(w)
+    pw = ops.process_weights(wq, ws)
+    bias = _dev_bf16(p.bias, dev)
+    del w, wq, ws
+    peaks, _ = _peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    res = {}
+    for M in (1, 4, 16, 64):
+        x = _dev_bf16(p.x[0, :M], dev)
+        out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
+        for _ in range(5):
+            ops.linear(x, pw, bias, out=out, workspace=wsb)
+            flush.zero_()
+        evs = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ops.linear(x, pw, bias, out=out, workspace=wsb)
+            b.record(stream)
+            flush.zero_()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        nbytes = p.N * p.K + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N + 2 * p.N
+        res[f"M{M}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                        "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm}
+    ops.check()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * mxfp8.h - C ABI of libmxfp8.so, the GB300 (sm_103a) W8A8 MXFP8 linear layer.
+ *
+ * The layer (sources are vLLM API pages, cited by page and section):
+ *   - "CompressedTensorsW8A8Mxfp8" (compressed_tensors_w8a8_mxfp8 page), class
+ *     docstring "MXFP8 format": FP8 E4M3 elements, one uint8 E8M0 scale per
+ *     32 consecutive elements along K, activations quantised at run time;
+ *     create_weights: weight [N, K] E4M3, weight_scale [N, K/32] uint8.
+ *   - "AiterFlyDSLMxfp8LinearKernel" (aiter_flydsl page), class docstring and
+ *     apply_weights: activation scales row-major [M, K/32]; the activation is
+ *     either quantised inside the layer or handed over pre-quantised; output
+ *     in the input dtype (bf16), then "+ bias".
+ *   - "Mxfp8LinearLayerConfig" (Mxfp8LinearKernel page): weight_shape (N, K)
+ *     and bmm_batch_size (a batched layer).
+ *   - "Mxfp8LinearKernel.process_weights_after_loading" (Mxfp8LinearKernel
+ *     page): a one-time rewrite of the weights after loading.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device (or managed) pointers on the
+ *     current device; the caller allocates and frees every buffer, including
+ *     the workspace.  The library allocates no memory and keeps no per-layer
+ *     state.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and returns without synchronising.  Nothing throws across the ABI.
+ *   - Argument problems are found before any launch and return
+ *     MXFP8_ERR_INVALID_ARG or MXFP8_ERR_UNSUPPORTED; a device that is not
+ *     sm_103 returns MXFP8_ERR_ARCH; a failed CUDA call returns MXFP8_ERR_CUDA.
+ *     mxfp8_last_error() then describes the problem (thread-local text).
+ *   - Every wait inside a kernel is bounded in time.  A wait that runs out sets
+ *     a device status word and the kernel returns; mxfp8_check() reports it as
+ *     MXFP8_ERR_TIMEOUT.
+ *   - Sizes are element counts.  Tensors are row-major and dense.
+ *   - E4M3 codes and E8M0 scales are passed as bytes (uint8_t).  bf16 values are
+ *     passed as raw 16-bit patterns (const void*).
+ */
+#ifndef MXFP8_H
+#define MXFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* mxfp8_stream_t;
+
+typedef enum {
+  MXFP8_OK = 0,
+  MXFP8_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer      */
+  MXFP8_ERR_UNSUPPORTED = 2, /* valid request this library does not implement */
+  MXFP8_ERR_ARCH = 3,        /* current device is not sm_103                   */
+  MXFP8_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed           */
+  MXFP8_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out               */
+} mxfp8_status;
+
+#define MXFP8_BLOCK_SIZE 32
+
+/* Text for the last non-OK status returned on this thread ("" if none). */
+const char* mxfp8_last_error(void);
+
+/* ABI version, currently 1. */
+int mxfp8_version(void);
+
+/*
+ * mxfp8_quantize - dynamic MXFP8 quantisation of bf16 rows.
+ *   Source: "AiterFlyDSLMxfp8LinearKernel.apply_weights" (aiter_flydsl page),
+ *   the mxfp8_e4m3_quantize step and its scale-shape assert; arithmetic per the
+ *   OCP MX v1.0 rule (section 6.3): per 32-block, e = floor(log2 amax) - 8
+ *   clamped to [-127, 127], scale byte = e + 127, element = E4M3(x / 2^e) with
+ *   round-to-nearest-even and saturation to +-448.  An all-zero block gets
+ *   scale byte 0; a block holding Inf or NaN gets 0xFF and elements 0x7F.
+ *   x_bf16  : device, [rows, K] bf16, 16-byte aligned.
+ *   x_q     : device, [rows, K] E4M3 codes out, 16-byte aligned.
+ *   x_scale : device, [rows, K/32] E8M0 bytes out (row-major).
+ *   rows >= 0 (0 is a no-op), K > 0 and K % 32 == 0.
+ */
+mxfp8_status mxfp8_quantize(const void* x_bf16, int64_t rows, int64_t K, uint8_t* x_q,
+                            uint8_t* x_scale, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_packed_sizes - bytes of the packed weight blobs written by
+ * mxfp8_process_weights for B batches of an [N, K] layer (B = 1 when not
+ * batched).  The sizes depend only on (B, N, K), so callers may persist and
+ * reload the blobs as plain bytes.
+ */
+mxfp8_status mxfp8_packed_sizes(int64_t B, int64_t N, int64_t K, size_t* w_bytes,
+                                size_t* sf_bytes);
+
+/*
+ * mxfp8_process_weights - one-time repack of loaded MXFP8 weights.
+ *   Source: "Mxfp8LinearKernel.process_weights_after_loading" (Mxfp8LinearKernel
+ *   page) and "CompressedTensorsW8A8Mxfp8.create_weights" (weight [N, K] E4M3,
+ *   weight_scale [N, K/32] uint8).
+ *   w        : device, [B, N, K] E4M3 codes (row-major, K contiguous).
+ *   w_scale  : device, [B, N, K/32] E8M0 bytes (row-major).
+ *   w_packed : device, w_bytes out: the E4M3 codes, K-major as the tensor cores
+ *              read them (the same bytes as w; w_packed == w is allowed).
+ *   sf_packed: device, sf_bytes out: the scales in 512-byte atoms of 128 rows x
+ *              4 blocks, the tensor cores' scale-factor layout; padding is zero.
+ *   B >= 1, N > 0, K > 0, K % 32 == 0.  Pointers 16-byte aligned.
+ */
+mxfp8_status mxfp8_process_weights(const uint8_t* w, const uint8_t* w_scale, int64_t B,
+                                   int64_t N, int64_t K, uint8_t* w_packed,
+                                   uint8_t* sf_packed, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_unpack_scales - exact inverse of the scale part of
+ * mxfp8_process_weights: sf_packed -> row-major [B, N, K/32].  Used to check
+ * the repack bit for bit (like row_major_weight on the aiter_flydsl page, which
+ * inverts that backend's weight shuffle).
+ */
+mxfp8_status mxfp8_unpack_scales(const uint8_t* sf_packed, int64_t B, int64_t N, int64_t K,
+                                 uint8_t* w_scale, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_workspace_size - device workspace bytes mxfp8_linear needs for this
+ * problem.  x_is_quantized = 1 when the caller passes x_q/x_scale.
+ */
+mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
+                                  int x_is_quantized, size_t* bytes);
+
+/*
+ * mxfp8_linear - out[b, m, n] = bf16( sum_k deq(x)[b, m, k] * deq(w)[b, n, k]
+ *                                     + bias[n] ).
+ *   Source: "AiterFlyDSLMxfp8LinearKernel.apply_weights" (aiter_flydsl page):
+ *   quantise x (or take the pre-quantised QuantizedActivation data/scale),
+ *   block-scaled GEMM against the processed weight, output in the input dtype,
+ *   then + bias; "Mxfp8LinearLayerConfig.bmm_batch_size" for B > 1 (B
+ *   independent products, one shared bias).
+ *   Exactly one input form:
+ *     x_bf16            : device, [B, M, K] bf16 (quantised inside the call), or
+ *     x_q and x_scale   : device, [B, M, K] E4M3 and [B, M, K/32] E8M0 row-major.
+ *   w_packed, sf_packed : device, from mxfp8_process_weights with the same B, N, K.
+ *   bias_bf16           : device, [N] bf16, or NULL for no bias.
+ *   out_bf16            : device, [B, M, N] bf16 out.
+ *   workspace           : device, >= mxfp8_workspace_size() bytes (may be NULL
+ *                         when that size is 0); 256-byte aligned.
+ *   The accumulation is fp32 on the tensor cores and the result is rounded once
+ *   to bf16 after the bias add.  Requirements: B >= 1, M >= 0 (0 is a no-op),
+ *   N > 0 with N % 8 == 0, K > 0 with K % 128 == 0 (else MXFP8_ERR_UNSUPPORTED),
+ *   all pointers 16-byte aligned.
+ */
+mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,
+                          int64_t B, int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
+                          const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                          void* workspace, size_t workspace_bytes, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_linear_path - mxfp8_linear with the kernel path chosen by the caller
+ * instead of by M: path 0 = automatic (as mxfp8_linear), 1 = small-M path
+ * (quantisation fused into the GEMM, weights on the MMA's M side), 2 = large-M
+ * path (separate quantise kernel, then the GEMM).  Both paths compute the same
+ * function; this exists so that tests can check each on every shape.
+ * Path 1 needs M <= 64 and x_bf16 (else MXFP8_ERR_UNSUPPORTED).
+ */
+mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
+                               const uint8_t* x_scale, int64_t B, int64_t M, int64_t N,
+                               int64_t K, const uint8_t* w_packed, const uint8_t* sf_packed,
+                               const void* bias_bf16, void* out_bf16, void* workspace,
+                               size_t workspace_bytes, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_quantize_packed - mxfp8_quantize for B batches of [M, K] rows, writing
+ * the scales straight into the packed atom layout the GEMM reads (the same
+ * layout mxfp8_process_weights gives weight scales; sf bytes as returned by
+ * mxfp8_packed_sizes(B, M, K)).  Padding bytes of the last row tile are not
+ * written.  This is the first half of mxfp8_linear on bf16 input.
+ *   x_bf16 : device, [B, M, K] bf16.   x_q : device, [B, M, K] out.
+ *   sfa_packed : device, packed scale atoms out.  K % 32 == 0, 16-byte aligned.
+ */
+mxfp8_status mxfp8_quantize_packed(const void* x_bf16, int64_t B, int64_t M, int64_t K,
+                                   uint8_t* x_q, uint8_t* sfa_packed, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_pack_scales - row-major E8M0 scales [B, R, K/32] -> packed atoms
+ * (zero padding), for any operand; mxfp8_process_weights uses it for weight
+ * scales and mxfp8_linear for pre-quantised activation scales.
+ */
+mxfp8_status mxfp8_pack_scales(const uint8_t* scale, int64_t B, int64_t R, int64_t K,
+                               uint8_t* sf_packed, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_gemm_packed - the block-scaled GEMM and epilogue alone, both operands
+ * already packed: out = bf16(x_q . w^T (block-scaled) + bias).  The second half
+ * of mxfp8_linear.  Requirements as for mxfp8_linear (N % 8 == 0, K % 128 == 0).
+ *   x_q, sfa_packed : device, from mxfp8_quantize_packed (or mxfp8_pack_scales).
+ *   w_packed, sf_packed : device, from mxfp8_process_weights.
+ */
+mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
+                               int64_t N, int64_t K, const uint8_t* w_packed,
+                               const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                               mxfp8_stream_t stream);
+
+/*
+ * mxfp8_check - synchronise `stream`, then read and clear the device status
+ * word of the current device.  Returns MXFP8_ERR_TIMEOUT if a bounded wait in
+ * any kernel of this library ran out since the last check, MXFP8_ERR_CUDA if
+ * the stream reports an error, else MXFP8_OK.
+ */
+mxfp8_status mxfp8_check(mxfp8_stream_t stream);
+
+/*
+ * mxfp8_debug_expire_wait - launch one tiny kernel whose mbarrier wait can
+ * never complete (nothing arrives), bounded by timeout_ns nanoseconds
+ * (1e3 <= timeout_ns <= 1e10).  The kernel records the expiry in the status
+ * word and returns, so that tests can see the timeout path work end to end
+ * (mxfp8_check then returns MXFP8_ERR_TIMEOUT).  No counterpart on the pages.
+ */
+mxfp8_status mxfp8_debug_expire_wait(uint64_t timeout_ns, mxfp8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_H */

@@ -1,0 +1,349 @@
+// api.cu - the C ABI of libmxfp8.so (declared in include/mxfp8.h).
+//
+// Host-side only: argument checks (all before any launch), workspace carving,
+// and the choice between the two linear paths.  The pages' kernel interface
+// ("Mxfp8LinearKernel": is_supported / can_implement / process_weights_after_
+// loading / apply_weights) maps onto it as: is_supported -> MXFP8_ERR_ARCH,
+// can_implement -> MXFP8_ERR_UNSUPPORTED, process_weights_after_loading ->
+// mxfp8_process_weights, apply_weights -> mxfp8_linear.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/mxfp8.h"
+#include "mx_kernels.h"
+#include "mx_layout.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mxfp8_status fail(mxfp8_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mxfp8_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MXFP8_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Current device, checked to be sm_103.  Returns MXFP8_OK and fills *sms.
+mxfp8_status current_device(int* sms) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MXFP8_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ok) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ok = true;
+  }
+  if (d.major != 10 || d.minor != 3)
+    return fail(MXFP8_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                d.major, d.minor);
+  *sms = d.sms;
+  return MXFP8_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+constexpr int kSmallM = 64;  // largest M the fused small-M path serves
+
+struct WsLayout {
+  int64_t xq_off, xq_bytes, sfa_off, sfa_bytes, total;
+};
+
+WsLayout prefill_workspace(int64_t B, int64_t M, int64_t K, bool quantized) {
+  WsLayout w;
+  w.xq_off = 0;
+  w.xq_bytes = quantized ? 0 : round_up(B * M * K, 256);
+  w.sfa_off = w.xq_bytes;
+  w.sfa_bytes = round_up(mx::sf_packed_bytes(B, M, K), 256);
+  w.total = w.xq_bytes + w.sfa_bytes;
+  return w;
+}
+
+mxfp8_status check_weights_args(const void* w, const void* ws, int64_t B, int64_t N, int64_t K) {
+  if (w == nullptr || ws == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null weight pointer");
+  if (B < 1 || N < 1 || K < 1) return fail(MXFP8_ERR_INVALID_ARG, "B=%lld N=%lld K=%lld", (long long)B, (long long)N, (long long)K);
+  if (K % 32 != 0) return fail(MXFP8_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
+  return MXFP8_OK;
+}
+
+mxfp8_status check_gemm_args(int64_t B, int64_t M, int64_t N, int64_t K) {
+  if (B < 1 || M < 0 || N < 1 || K < 1)
+    return fail(MXFP8_ERR_INVALID_ARG, "B=%lld M=%lld N=%lld K=%lld", (long long)B, (long long)M,
+                (long long)N, (long long)K);
+  if (K % 32 != 0) return fail(MXFP8_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
+  if (K % 128 != 0)
+    return fail(MXFP8_ERR_UNSUPPORTED, "K=%lld: this library needs K %% 128 == 0", (long long)K);
+  if (N % 8 != 0)
+    return fail(MXFP8_ERR_UNSUPPORTED, "N=%lld: this library needs N %% 8 == 0", (long long)N);
+  if (B * M > (1ll << 31) || N > (1ll << 30) || K > (1ll << 30))
+    return fail(MXFP8_ERR_UNSUPPORTED, "problem too large");
+  return MXFP8_OK;
+}
+
+}  // namespace
+
+namespace mx {
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace mx
+
+extern "C" {
+
+const char* mxfp8_last_error(void) { return g_last_error.c_str(); }
+
+int mxfp8_version(void) { return 1; }
+
+mxfp8_status mxfp8_quantize(const void* x_bf16, int64_t rows, int64_t K, uint8_t* x_q,
+                            uint8_t* x_scale, mxfp8_stream_t stream) {
+  if (rows < 0 || K < 1) return fail(MXFP8_ERR_INVALID_ARG, "rows=%lld K=%lld", (long long)rows, (long long)K);
+  if (K % 32 != 0) return fail(MXFP8_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
+  if (rows == 0) return MXFP8_OK;
+  if (x_bf16 == nullptr || x_q == nullptr || x_scale == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x_bf16, 16) || !aligned(x_q, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "x_bf16 and x_q must be 16-byte aligned");
+  int sms = 0;
+  mxfp8_status st = current_device(&sms);
+  if (st != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_quantize(x_bf16, rows, K, x_q, x_scale, false, 1, rows, sms,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_packed_sizes(int64_t B, int64_t N, int64_t K, size_t* w_bytes, size_t* sf_bytes) {
+  if (w_bytes == nullptr || sf_bytes == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  if (B < 1 || N < 1 || K < 1 || K % 32 != 0)
+    return fail(MXFP8_ERR_INVALID_ARG, "B=%lld N=%lld K=%lld", (long long)B, (long long)N, (long long)K);
+  *w_bytes = static_cast<size_t>(B * N * K);
+  *sf_bytes = static_cast<size_t>(mx::sf_packed_bytes(B, N, K));
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_process_weights(const uint8_t* w, const uint8_t* w_scale, int64_t B, int64_t N,
+                                   int64_t K, uint8_t* w_packed, uint8_t* sf_packed,
+                                   mxfp8_stream_t stream) {
+  mxfp8_status st = check_weights_args(w, w_scale, B, N, K);
+  if (st != MXFP8_OK) return st;
+  if (w_packed == nullptr || sf_packed == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned(w, 16) || !aligned(w_packed, 16) || !aligned(sf_packed, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "w, w_packed and sf_packed must be 16-byte aligned");
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (w_packed != w) {
+    cudaError_t e = cudaMemcpyAsync(w_packed, w, static_cast<size_t>(B * N * K), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "weight copy");
+  }
+  cudaError_t e = mx::launch_sf_pack(w_scale, B, N, K, sf_packed, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "scale repack launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_unpack_scales(const uint8_t* sf_packed, int64_t B, int64_t N, int64_t K,
+                                 uint8_t* w_scale, mxfp8_stream_t stream) {
+  mxfp8_status st = check_weights_args(sf_packed, w_scale, B, N, K);
+  if (st != MXFP8_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_sf_unpack(sf_packed, B, N, K, w_scale, sms,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scale unpack launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, int x_is_quantized,
+                                  size_t* bytes) {
+  if (bytes == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  if (B < 1 || M < 0 || N < 1 || K < 1 || K % 32 != 0)
+    return fail(MXFP8_ERR_INVALID_ARG, "B=%lld M=%lld N=%lld K=%lld", (long long)B, (long long)M,
+                (long long)N, (long long)K);
+  *bytes = static_cast<size_t>(prefill_workspace(B, M, K, x_is_quantized != 0).total);
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
+                               const uint8_t* x_scale, int64_t B, int64_t M, int64_t N, int64_t K,
+                               const uint8_t* w_packed, const uint8_t* sf_packed,
+                               const void* bias_bf16, void* out_bf16, void* workspace,
+                               size_t workspace_bytes, mxfp8_stream_t stream) {
+  if (path < 0 || path > 2) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
+  {
+    mxfp8_status ck = check_gemm_args(B, M, N, K);
+    if (ck != MXFP8_OK) return ck;
+  }
+  if (M == 0) return MXFP8_OK;  // nothing to read or write; pointers may be null
+  const bool have_x = x_bf16 != nullptr;
+  const bool have_q = x_q != nullptr || x_scale != nullptr;
+  if (have_x == have_q)
+    return fail(MXFP8_ERR_INVALID_ARG, "pass exactly one of x_bf16 or (x_q, x_scale)");
+  if (have_q && (x_q == nullptr || x_scale == nullptr))
+    return fail(MXFP8_ERR_INVALID_ARG, "x_q and x_scale must both be given");
+  if (w_packed == nullptr || sf_packed == nullptr || out_bf16 == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null weight or output pointer");
+  if (!aligned(w_packed, 16) || !aligned(sf_packed, 16) || !aligned(out_bf16, 16) ||
+      (have_x && !aligned(x_bf16, 16)) || (have_q && !aligned(x_q, 16)) ||
+      (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
+    return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (M == 0) return MXFP8_OK;
+  int sms = 0;
+  mxfp8_status st = current_device(&sms);
+  if (st != MXFP8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (path == 1) return fail(MXFP8_ERR_UNSUPPORTED, "the small-M fused path is not built yet");
+  (void)kSmallM;
+
+  const WsLayout ws = prefill_workspace(B, M, K, have_q);
+  if (static_cast<int64_t>(workspace_bytes) < ws.total)
+    return fail(MXFP8_ERR_INVALID_ARG, "workspace has %zu bytes, needs %lld", workspace_bytes,
+                (long long)ws.total);
+  if (workspace == nullptr || !aligned(workspace, 256))
+    return fail(MXFP8_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  uint8_t* sfa = wsb + ws.sfa_off;
+  const uint8_t* a = x_q;
+  cudaError_t e;
+  if (have_x) {
+    uint8_t* xq = wsb + ws.xq_off;
+    e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    a = xq;
+  } else {
+    e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
+  }
+  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K};
+  const char* msg = "";
+  e = mx::launch_gemm_prefill(p, sms, s, &msg);
+  if (e != cudaSuccess) return cuda_fail(e, msg);
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale, int64_t B,
+                          int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
+                          const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                          void* workspace, size_t workspace_bytes, mxfp8_stream_t stream) {
+  return mxfp8_linear_path(0, x_bf16, x_q, x_scale, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                           out_bf16, workspace, workspace_bytes, stream);
+}
+
+mxfp8_status mxfp8_quantize_packed(const void* x_bf16, int64_t B, int64_t M, int64_t K,
+                                   uint8_t* x_q, uint8_t* sfa_packed, mxfp8_stream_t stream) {
+  if (B < 1 || M < 0 || K < 1 || K % 32 != 0)
+    return fail(MXFP8_ERR_INVALID_ARG, "B=%lld M=%lld K=%lld", (long long)B, (long long)M, (long long)K);
+  if (M == 0) return MXFP8_OK;
+  if (x_bf16 == nullptr || x_q == nullptr || sfa_packed == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x_bf16, 16) || !aligned(x_q, 16) || !aligned(sfa_packed, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  int sms = 0;
+  mxfp8_status st = current_device(&sms);
+  if (st != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_quantize(x_bf16, B * M, K, x_q, sfa_packed, true, B, M, sms,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_pack_scales(const uint8_t* scale, int64_t B, int64_t R, int64_t K,
+                               uint8_t* sf_packed, mxfp8_stream_t stream) {
+  mxfp8_status st = check_weights_args(scale, sf_packed, B, R, K);
+  if (st != MXFP8_OK) return st;
+  if (!aligned(sf_packed, 16)) return fail(MXFP8_ERR_INVALID_ARG, "sf_packed must be 16-byte aligned");
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_sf_pack(scale, B, R, K, sf_packed, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scale repack launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
+                               int64_t N, int64_t K, const uint8_t* w_packed,
+                               const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                               mxfp8_stream_t stream) {
+  mxfp8_status st = check_gemm_args(B, M, N, K);
+  if (st != MXFP8_OK) return st;
+  if (x_q == nullptr || sfa_packed == nullptr || w_packed == nullptr || sf_packed == nullptr ||
+      out_bf16 == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x_q, 16) || !aligned(sfa_packed, 16) || !aligned(w_packed, 16) ||
+      !aligned(sf_packed, 16) || !aligned(out_bf16, 16) ||
+      (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
+    return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (M == 0) return MXFP8_OK;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  mx::GemmProblem p{x_q, w_packed, sfa_packed, sf_packed, bias_bf16, out_bf16, B, M, N, K};
+  const char* msg = "";
+  cudaError_t e = mx::launch_gemm_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream), &msg);
+  if (e != cudaSuccess) return cuda_fail(e, msg);
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_check(mxfp8_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int s1 = 0, s2 = 0, s3 = 0;
+  if ((e = mx::take_status_quantize(&s1)) != cudaSuccess ||
+      (e = mx::take_status_gemm(&s2)) != cudaSuccess ||
+      (e = mx::take_status_debug(&s3)) != cudaSuccess)
+    return cuda_fail(e, "status word read");
+  if ((s1 | s2 | s3) & 1u) return fail(MXFP8_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_debug_expire_wait(uint64_t timeout_ns, mxfp8_stream_t stream) {
+  if (timeout_ns < 1000 || timeout_ns > 10000000000ull)
+    return fail(MXFP8_ERR_INVALID_ARG, "timeout_ns=%llu out of [1e3, 1e10]", (unsigned long long)timeout_ns);
+  int sms = 0;
+  mxfp8_status st = current_device(&sms);
+  if (st != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_expire_wait(timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "debug kernel launch");
+  return MXFP8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// mx_kernels.h - host-side launchers shared between the translation units of
+// libmxfp8.so.  Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mx {
+
+// quantize.cu
+cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                            bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
+                            cudaStream_t stream);
+cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
+                           int sms, cudaStream_t stream);
+cudaError_t launch_sf_unpack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
+                             int sms, cudaStream_t stream);
+cudaError_t take_status_quantize(unsigned int* out);
+
+// gemm.cu: the large-M path.  A = activations [B, M, K] E4M3, Bw = weights
+// [B, N, K] E4M3, both K-major; sfa / sfb are packed scale atoms.
+struct GemmProblem {
+  const uint8_t* a;
+  const uint8_t* w;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const void* bias;  // bf16 [N] or nullptr
+  void* out;         // bf16 [B, M, N]
+  int64_t B, M, N, K;
+};
+// Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
+cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
+cudaError_t take_status_gemm(unsigned int* out);
+
+// debug.cu
+cudaError_t launch_expire_wait(uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t take_status_debug(unsigned int* out);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved once, via the runtime).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+}  // namespace mx

@@ -1,0 +1,41 @@
+// mx_layout.cuh - byte layout of the packed scale factors.
+//
+// The tensor cores read block scales from tensor memory; tcgen05.cp fills
+// tensor memory from 512-byte shared-memory "atoms".  An atom holds the E8M0
+// scales of 128 rows x 4 consecutive 32-element blocks along K (one 128-wide
+// K tile).  Within an atom, row r (0..127) and block j (0..3) sit at
+//     (r % 32) * 16 + (r / 32) * 4 + j
+// so each 16-byte line carries rows {i, i+32, i+64, i+96}.
+//
+// Atoms are stored K-tile major, then row-tile:
+//     atom(b, kt, rt) = (b * KT + kt) * RT + rt,   RT = ceil(R / 128),
+//                                                  KT = ceil(K / 128)
+// so the atoms of consecutive 128-row tiles at one K tile are adjacent, and a
+// 256-row operand tile reads 1 KB contiguous per K tile.  Rows >= R and blocks
+// >= K/32 are padding and hold 0.
+#pragma once
+
+#include <stdint.h>
+
+namespace mx {
+
+constexpr int kAtomRows = 128;
+constexpr int kAtomBlocks = 4;
+constexpr int kAtomBytes = 512;
+constexpr int kTileK = 128;  // K elements covered by one atom column group
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+__host__ __device__ __forceinline__ int64_t sf_packed_bytes(int64_t B, int64_t R, int64_t K) {
+  return B * ceil_div(K, kTileK) * ceil_div(R, kAtomRows) * kAtomBytes;
+}
+
+// Offset of the scale of (batch b, row r, block kb) inside the packed buffer.
+__host__ __device__ __forceinline__ int64_t sf_packed_offset(int64_t b, int64_t r, int64_t kb,
+                                                            int64_t RT, int64_t KT) {
+  const int64_t kt = kb >> 2, j = kb & 3;
+  const int64_t rt = r >> 7, rr = r & 127;
+  return ((b * KT + kt) * RT + rt) * kAtomBytes + (rr & 31) * 16 + (rr >> 5) * 4 + j;
+}
+
+}  // namespace mx

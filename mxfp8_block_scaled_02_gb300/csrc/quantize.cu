@@ -1,0 +1,191 @@
+// quantize.cu - dynamic MXFP8 quantisation and the scale-factor repack.
+//
+// Quantisation rule (OCP MX v1.0, section 6.3, for the MXFP8 format of the
+// "CompressedTensorsW8A8Mxfp8" page): per 32-element block along K the scale
+// exponent is floor(log2 amax) - 8, clamped to [-127, 127]; each element is
+// x / 2^e rounded to E4M3, nearest-even, saturating to +-448.
+//
+// Everything is decided on the bf16 bit patterns:
+//   * |x| as an integer is (bits & 0x7FFF); for non-negative floats integer
+//     order is value order, and NaN/Inf are exactly the patterns >= 0x7F80.
+//   * for a finite amax with biased exponent field E (E = 0 for zero and
+//     subnormals) floor(log2 amax) = E - 127, so the scale byte is
+//     max(E - 8, 0); every subnormal or zero block clamps to byte 0.
+//   * 2^-e = 2^(127 - byte) is a normal fp32 for byte in [0, 246], and x * 2^-e
+//     is exact in fp32 unless it underflows, in which case the result rounds
+//     to a signed zero in E4M3 either way.
+//   * the fp32 -> E4M3 rounding is the hardware's cvt.rn.satfinite.e4m3x2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mx_kernels.h"
+#include "mx_layout.cuh"
+#include "mx_ptx.cuh"
+
+namespace mx {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kQuantUnroll = 4;  // independent 32-blocks in flight per group of 4 lanes
+
+// Four lanes share one 32-element block; each lane owns 8 consecutive values.
+// kPacked selects the scale output: false = row-major [rows, K/32], true = the
+// 512-byte atom layout of mx_layout.cuh (rows grouped per batch of rows_per_b).
+template <bool kPacked>
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
+    const uint4* __restrict__ x, int64_t nblocks, int64_t KB, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int64_t rows_per_b, int64_t RT, int64_t KT) {
+  const int lane = threadIdx.x & 31;
+  const int part = lane & 3;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  constexpr int64_t kPerWarp = 8 * kQuantUnroll;
+
+  for (int64_t base = warp * kPerWarp; base < nblocks; base += nwarps * kPerWarp) {
+    uint4 v[kQuantUnroll];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t blk = base + u * 8 + (lane >> 2);
+      v[u] = blk < nblocks ? __ldg(x + blk * 4 + part) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t blk = base + u * 8 + (lane >> 2);
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t amax = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+
+      const bool nonfinite = amax >= 0x7F80u;
+      const uint32_t E = amax >> 7;
+      const uint32_t sbyte = nonfinite ? 0xFFu : (E > 8u ? E - 8u : 0u);
+      const float mul = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);
+
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16) * mul;
+        const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * mul;
+        c[i] = cvt_e4m3x2(lo, hi);
+      }
+      uint2 out = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      if (nonfinite) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+
+      if (blk < nblocks) {
+        *reinterpret_cast<uint2*>(q + blk * 32 + part * 8) = out;
+        if (part == 0) {
+          if (kPacked) {
+            const int64_t row = blk / KB, kb = blk - row * KB;
+            const int64_t b = row / rows_per_b, r = row - b * rows_per_b;
+            s[sf_packed_offset(b, r, kb, RT, KT)] = static_cast<uint8_t>(sbyte);
+          } else {
+            s[blk] = static_cast<uint8_t>(sbyte);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Row-major [B, R, KB] -> packed atoms; one thread per 4 output bytes (the 4
+// blocks of one row inside an atom).  Padding rows/blocks are written as 0.
+__global__ void __launch_bounds__(256) sf_pack_kernel(const uint8_t* __restrict__ src, int64_t R,
+                                                       int64_t KB, int64_t RT, int64_t KT,
+                                                       uint32_t* __restrict__ dst, int64_t nwords) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t wi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; wi < nwords;
+       wi += stride) {
+    const int64_t atom = wi >> 7;          // 128 words per 512-byte atom
+    const int within = static_cast<int>(wi & 127);
+    const int line = within >> 2, grp = within & 3;
+    const int64_t rt = atom % RT;
+    const int64_t kt = (atom / RT) % KT;
+    const int64_t b = atom / (RT * KT);
+    const int64_t r = rt * kAtomRows + grp * 32 + line;
+    uint32_t v = 0;
+    if (r < R) {
+      const uint8_t* row = src + (b * R + r) * KB;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t kb = kt * 4 + j;
+        if (kb < KB) v |= static_cast<uint32_t>(row[kb]) << (8 * j);
+      }
+    }
+    dst[wi] = v;
+  }
+}
+
+// Packed atoms -> row-major [B, R, KB]; one thread per output byte.
+__global__ void __launch_bounds__(256) sf_unpack_kernel(const uint8_t* __restrict__ src, int64_t B,
+                                                         int64_t R, int64_t KB, int64_t RT,
+                                                         int64_t KT, uint8_t* __restrict__ dst) {
+  const int64_t n = B * R * KB;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t kb = i % KB;
+    const int64_t r = (i / KB) % R;
+    const int64_t b = i / (KB * R);
+    dst[i] = src[sf_packed_offset(b, r, kb, RT, KT)];
+  }
+}
+
+int grid_for(int64_t work_items, int threads, int sms, int per_sm) {
+  int64_t g = (work_items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                            bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
+                            cudaStream_t stream) {
+  const int64_t nblocks = rows * (K / 32);
+  if (nblocks == 0) return cudaSuccess;
+  const int64_t threads_needed = (nblocks + kQuantUnroll - 1) / kQuantUnroll * 4;
+  const int grid = grid_for(threads_needed, kQuantThreads, sms, 8);
+  const int64_t KB = K / 32;
+  const int64_t RT = ceil_div(rows_per_b, kAtomRows), KT = ceil_div(K, kTileK);
+  (void)B;
+  if (packed_scales)
+    quantize_kernel<true><<<grid, kQuantThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), nblocks, KB, q, s, rows_per_b, RT, KT);
+  else
+    quantize_kernel<false><<<grid, kQuantThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), nblocks, KB, q, s, rows_per_b, RT, KT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
+                           int sms, cudaStream_t stream) {
+  const int64_t KB = K / 32, RT = ceil_div(R, kAtomRows), KT = ceil_div(K, kTileK);
+  const int64_t nwords = sf_packed_bytes(B, R, K) / 4;
+  if (nwords == 0) return cudaSuccess;
+  sf_pack_kernel<<<grid_for(nwords, 256, sms, 8), 256, 0, stream>>>(
+      src, R, KB, RT, KT, reinterpret_cast<uint32_t*>(dst), nwords);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_unpack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
+                             int sms, cudaStream_t stream) {
+  const int64_t KB = K / 32, RT = ceil_div(R, kAtomRows), KT = ceil_div(K, kTileK);
+  const int64_t n = B * R * KB;
+  if (n == 0) return cudaSuccess;
+  sf_unpack_kernel<<<grid_for(n, 256, sms, 8), 256, 0, stream>>>(src, B, R, KB, RT, KT, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t take_status_quantize(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mx

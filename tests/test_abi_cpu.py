@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+symbol, and rejects bad arguments before touching a device."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+from mxfp8_block_scaled_02_gb300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp8.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp8_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["mxfp8_quantize", "mxfp8_process_weights", "mxfp8_linear",
+                     "mxfp8_packed_sizes", "mxfp8_workspace_size", "mxfp8_last_error",
+                     "mxfp8_check"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(mxfp8_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # the binding covers exactly the declared calls
+    assert set(ops.SIGNATURES) == set(declared_functions())
+
+
+def test_version_and_sizes(lib):
+    assert lib.mxfp8_version() == 1
+    assert ops.packed_sizes(1, 256, 512) == (256 * 512, 2 * 4 * 512)
+    assert ops.packed_sizes(16, 512, 7168) == (16 * 512 * 7168, 16 * 56 * 4 * 512)
+    # ragged rows and K round up to whole atoms
+    assert ops.packed_sizes(1, 129, 160) == (129 * 160, 2 * 2 * 512)
+    assert ops.workspace_size(1, 4096, 14336, 4096, False) == 4096 * 4096 + 32 * 32 * 512
+    assert ops.workspace_size(1, 8192, 4096, 14336, True) == 64 * 112 * 512
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+def test_argument_errors_are_reported_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every call below fails its checks first
+    # neither or both activation forms
+    st = lib.mxfp8_linear(None, None, None, 1, 16, 256, 512, fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == 1 and b"exactly one" in lib.mxfp8_last_error()
+    st = lib.mxfp8_linear(fake, fake, fake, 1, 16, 256, 512, fake, fake, None, fake, fake, 1 << 20, None)
+    assert st == 1
+    # K not a multiple of 32 -> invalid; of 128 -> unsupported
+    assert lib.mxfp8_linear(fake, None, None, 1, 16, 256, 500, fake, fake, None, fake, fake, 1 << 20, None) == 1
+    assert lib.mxfp8_linear(fake, None, None, 1, 16, 256, 544, fake, fake, None, fake, fake, 1 << 20, None) == 2
+    # N not a multiple of 8
+    assert lib.mxfp8_linear(fake, None, None, 1, 16, 250, 512, fake, fake, None, fake, fake, 1 << 20, None) == 2
+    # misaligned output
+    assert lib.mxfp8_linear(fake, None, None, 1, 16, 256, 512, fake, fake, None, P(0x10002), fake,
+                            1 << 20, None) == 1
+    # bad path selector
+    assert lib.mxfp8_linear_path(7, fake, None, None, 1, 16, 256, 512, fake, fake, None, fake, fake,
+                                 1 << 20, None) == 1
+    # quantize: K % 32
+    assert lib.mxfp8_quantize(fake, 4, 33, fake, fake, None) == 1
+    assert lib.mxfp8_quantize(None, 4, 64, fake, fake, None) == 1
+    # process_weights: null scale
+    assert lib.mxfp8_process_weights(fake, None, 1, 8, 64, fake, fake, None) == 1
+    # sizes: bad K
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.mxfp8_packed_sizes(1, 8, 48, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert lib.mxfp8_debug_expire_wait(10, None) == 1
+
+
+def test_python_binding_validates_shapes():
+    with pytest.raises(TypeError):
+        ops.quantize(torch.zeros(4, 64, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        ops.quantize(torch.zeros(4, 64, dtype=torch.bfloat16))   # CPU tensor
+
+
+def test_build_entry_point_is_importable():
+    import __graft_entry__ as g
+    assert callable(g.build) and callable(g.smoke)
