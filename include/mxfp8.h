@@ -194,6 +194,37 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
                                mxfp8_stream_t stream);
 
 /*
+ * Size of the fixed device scratch array used by mxfp8_linear_noalloc.
+ */
+#define MXFP8_NOALLOC_SCRATCH_BYTES (32ll << 20)
+
+/*
+ * mxfp8_linear_noalloc - mxfp8_linear for bf16 input, for callers that cannot
+ * allocate device memory (no workspace argument).  No counterpart in the
+ * paper: the pages' layer always allocates its quantised activation.
+ *   Who needs it: a process whose GPU memory is already owned by another
+ *   allocator (a serving runtime that reserves the device at start-up, where a
+ *   new cudaMalloc fails or fragments that pool), or a runtime with a fixed
+ *   memory plan that forbids allocation after initialisation.
+ *   Scratch: a file-scope device array of MXFP8_NOALLOC_SCRATCH_BYTES (32 MiB)
+ *   inside the library, held by every GPU that loads the library until the
+ *   process exits.  The call needs round_up(B*M*K, 256) + round_up(packed
+ *   scale bytes of (B, M, K), 256) bytes of it and returns
+ *   MXFP8_ERR_UNSUPPORTED beyond that (e.g. M*K above ~32.5 M at B = 1).
+ *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  Every call shares the one array, so calls
+ *   that overlap on the GPU (different streams or threads) race and must be
+ *   serialised by the caller.
+ *   Arguments, layouts and requirements as for mxfp8_linear with x_bf16
+ *   (B >= 1, N % 8 == 0, K % 128 == 0, 16-byte aligned pointers).
+ */
+mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int64_t M, int64_t N, int64_t K,
+                                  const uint8_t* w_packed, const uint8_t* sf_packed,
+                                  const void* bias_bf16, void* out_bf16, mxfp8_stream_t stream);
+
+/*
  * mxfp8_check - synchronise `stream`, then read and clear the device status
  * word of the current device.  Returns MXFP8_ERR_TIMEOUT if a bounded wait in
  * any kernel of this library ran out since the last check, MXFP8_ERR_CUDA if

@@ -114,6 +114,8 @@ mxfp8_status check_gemm_args(int64_t B, int64_t M, int64_t N, int64_t K) {
 
 namespace mx {
 
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = [] {
     void* p = nullptr;

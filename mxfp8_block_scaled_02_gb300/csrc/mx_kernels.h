@@ -37,6 +37,9 @@ cudaError_t take_status_gemm(unsigned int* out);
 cudaError_t launch_expire_wait(uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t take_status_debug(unsigned int* out);
 
+// api.cu: record the text mxfp8_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 // Driver entry point for cuTensorMapEncodeTiled (resolved once, via the runtime).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -44,6 +44,7 @@ SIGNATURES = {
     "mxfp8_quantize_packed": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "mxfp8_pack_scales": (_INT, [_P, _I64, _I64, _I64, _P, _P]),
     "mxfp8_gemm_packed": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "mxfp8_linear_noalloc": (_INT, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "mxfp8_check": (_INT, [_P]),
     "mxfp8_debug_expire_wait": (_INT, [_U64, _P]),
 }
@@ -249,6 +250,33 @@ def gemm_packed(pa: PackedActivation, pw: PackedWeights, bias: torch.Tensor | No
     _check(load().mxfp8_gemm_packed(_ptr(pa.x_q), _ptr(pa.sf_packed), pa.B, pa.M, pw.N, pa.K,
                                     _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
                                     _stream()))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def linear_noalloc(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 linear that allocates no device workspace (mxfp8_linear_noalloc).
+
+    For callers that cannot allocate device memory: the library's fixed
+    32 MiB scratch array holds the quantised activations, so B*M*K is limited
+    (the call raises MXFP8_ERR_UNSUPPORTED beyond it).  Calls that overlap on
+    the GPU share that array and race.  Only ``out`` is allocated here when it
+    is not given.
+    """
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    _require_cuda(x, bias, out)
+    K = x.shape[-1]
+    if K != pw.K:
+        raise ValueError(f"x has K={K}, weights have K={pw.K}")
+    M = x.shape[1] if pw.batched else (x.numel() // K if K else 0)
+    if out is None:
+        out = torch.empty((*x.shape[:-1], pw.N), dtype=torch.bfloat16, device=x.device)
+    _check(load().mxfp8_linear_noalloc(_ptr(x), pw.B, M, pw.N, K, _ptr(pw.w_packed),
+                                       _ptr(pw.sf_packed), _ptr(bias), _ptr(out), _stream()))
     return out
 
 
