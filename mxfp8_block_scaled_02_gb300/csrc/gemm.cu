@@ -13,8 +13,11 @@
 //               TMEM) and tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 per
 //               instruction, 4 per 128-wide K tile, scale byte selected by the
 //               instruction descriptor's scale-factor id);
-//   warps 2..5  epilogue: tcgen05.ld the fp32 accumulator, + bias, round to
-//               bf16, store.
+//   warps 2..9  epilogue: two warps per 32-lane TMEM quarter, each copies its
+//               half of the fp32 accumulator row (BN/2 columns) into registers,
+//               hands the accumulator back to the MMA warp at once, then adds
+//               the bias, rounds to bf16 and stores while the next tile's
+//               main loop already runs.
 // Every wait is bounded (mx_ptx.cuh); on expiry the roles stop, the kernel
 // drains its own in-flight copies and frees its tensor memory.
 #include <cuda_bf16.h>
@@ -56,7 +59,10 @@ struct Cfg {
   static constexpr int T_SFB = T_SFA + STAGES * 4;
   static constexpr int T_END = T_SFB + STAGES * NB_ATOMS * 4;
   static constexpr int TMEM_COLS = T_END <= 256 ? 256 : 512;
-  static constexpr int THREADS = 192;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue thread
+  static constexpr int THREADS = 64 + EPI_THREADS;
   static_assert(T_END <= 512, "tensor memory overflow");
   static_assert(SMEM_ALLOC <= 232448, "shared memory overflow");
   static_assert(BN % 128 == 0 && BN <= 256, "BN");
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, C::EPI_THREADS);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -213,7 +219,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lane quarter this warp may access
+    const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+    const int col0 = ((warp - 2) >> 2) * C::EPI_COLS;
     const int row = quad * 32 + lane;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
@@ -221,45 +228,45 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tile_coords(tile, args, b, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
+      uint32_t r[C::EPI_COLS];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + col0;
+#pragma unroll
+      for (int c = 0; c < C::EPI_COLS / 32; ++c)
+        tmem_ld_32x32b_x32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(acc_empty);                  // accumulator free for the next tile
+      acc_phase ^= 1u;
+
       const int m = mt * BM + row;
-      __nv_bfloat16* orow = args.out + (static_cast<int64_t>(b) * args.M + m) * args.N;
-#pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + c * 32, r);
-        tmem_ld_wait();
-        const int n0 = nt * C::BN + c * 32;
-        if (m < args.M) {
+      if (m < args.M) {
+        __nv_bfloat16* orow = args.out + (static_cast<int64_t>(b) * args.M + m) * args.N;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int n = n0 + 8 * g;
-            if (n < args.N) {
-              float bv[8];
-              if (args.bias != nullptr) {
-                const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
-                const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+        for (int g = 0; g < C::EPI_COLS / 8; ++g) {
+          const int n = nt * C::BN + col0 + 8 * g;
+          if (n < args.N) {
+            float bv[8];
+            if (args.bias != nullptr) {
+              const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
+              const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  bv[2 * i] = __uint_as_float(bw[i] << 16);
-                  bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) bv[i] = 0.f;
+              for (int i = 0; i < 4; ++i) {
+                bv[2 * i] = __uint_as_float(bw[i] << 16);
+                bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
               }
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(r[8 * g + 0]) + bv[0], __uint_as_float(r[8 * g + 1]) + bv[1]);
-              o.y = pack_bf16x2(__uint_as_float(r[8 * g + 2]) + bv[2], __uint_as_float(r[8 * g + 3]) + bv[3]);
-              o.z = pack_bf16x2(__uint_as_float(r[8 * g + 4]) + bv[4], __uint_as_float(r[8 * g + 5]) + bv[5]);
-              o.w = pack_bf16x2(__uint_as_float(r[8 * g + 6]) + bv[6], __uint_as_float(r[8 * g + 7]) + bv[7]);
-              *reinterpret_cast<uint4*>(orow + n) = o;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) bv[i] = 0.f;
             }
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(r[8 * g + 0]) + bv[0], __uint_as_float(r[8 * g + 1]) + bv[1]);
+            o.y = pack_bf16x2(__uint_as_float(r[8 * g + 2]) + bv[2], __uint_as_float(r[8 * g + 3]) + bv[3]);
+            o.z = pack_bf16x2(__uint_as_float(r[8 * g + 4]) + bv[4], __uint_as_float(r[8 * g + 5]) + bv[5]);
+            o.w = pack_bf16x2(__uint_as_float(r[8 * g + 6]) + bv[6], __uint_as_float(r[8 * g + 7]) + bv[7]);
+            *reinterpret_cast<uint4*>(orow + n) = o;
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
     }
   }
 

@@ -28,31 +28,39 @@ namespace mx {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;  // independent 32-blocks in flight per group of 4 lanes
+constexpr int kQuantUnroll = 4;  // independent 8-block tasks in flight per warp
 
-// Four lanes share one 32-element block; each lane owns 8 consecutive values.
+// One warp task = 8 consecutive 32-element blocks of one row (256 values,
+// 512 bytes of bf16).  Lane l owns 8 values: block j = l / 4 of the task,
+// quarter l % 4 of that block; four lanes combine their amax by shuffles.
 // kPacked selects the scale output: false = row-major [rows, K/32], true = the
 // 512-byte atom layout of mx_layout.cuh (rows grouped per batch of rows_per_b).
+// All index arithmetic is warp-uniform 32-bit except the final byte offsets.
 template <bool kPacked>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
-    const uint4* __restrict__ x, int64_t nblocks, int64_t KB, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ s, int64_t rows_per_b, int64_t RT, int64_t KT) {
+    const uint4* __restrict__ x, uint32_t KB, uint32_t tasks_per_row, uint32_t ntasks,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT,
+    uint32_t KT) {
   const int lane = threadIdx.x & 31;
-  const int part = lane & 3;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  constexpr int64_t kPerWarp = 8 * kQuantUnroll;
+  const int j = lane >> 2, part = lane & 3;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
 
-  for (int64_t base = warp * kPerWarp; base < nblocks; base += nwarps * kPerWarp) {
+  for (uint32_t t0 = warp * kQuantUnroll; t0 < ntasks; t0 += nwarps * kQuantUnroll) {
     uint4 v[kQuantUnroll];
+    uint32_t row[kQuantUnroll], kb[kQuantUnroll];
+    bool valid[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t blk = base + u * 8 + (lane >> 2);
-      v[u] = blk < nblocks ? __ldg(x + blk * 4 + part) : make_uint4(0, 0, 0, 0);
+      const uint32_t t = t0 + u;
+      row[u] = t / tasks_per_row;
+      kb[u] = (t - row[u] * tasks_per_row) * 8 + j;
+      valid[u] = t < ntasks && kb[u] < KB;
+      const int64_t blk = static_cast<int64_t>(row[u]) * KB + kb[u];
+      v[u] = valid[u] ? __ldg(x + blk * 4 + part) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t blk = base + u * 8 + (lane >> 2);
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       uint32_t amax = 0;
 #pragma unroll
@@ -74,17 +82,34 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
       }
       uint2 out = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
       if (nonfinite) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      const int64_t blk = static_cast<int64_t>(row[u]) * KB + kb[u];
+      if (valid[u]) *reinterpret_cast<uint2*>(q + blk * 32 + part * 8) = out;
 
-      if (blk < nblocks) {
-        *reinterpret_cast<uint2*>(q + blk * 32 + part * 8) = out;
-        if (part == 0) {
-          if (kPacked) {
-            const int64_t row = blk / KB, kb = blk - row * KB;
-            const int64_t b = row / rows_per_b, r = row - b * rows_per_b;
-            s[sf_packed_offset(b, r, kb, RT, KT)] = static_cast<uint8_t>(sbyte);
-          } else {
-            s[blk] = static_cast<uint8_t>(sbyte);
-          }
+      // Scale bytes: gather the task's 8 bytes (lanes 0, 4, ..., 28) so that
+      // whole words are stored when the task is complete.
+      const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 0);
+      const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 4);
+      const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 8);
+      const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 12);
+      const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      const uint32_t kb_task = kb[u] - j;  // first block of the task
+      const bool full_task = kb_task + 8 <= KB;
+      if (kPacked) {
+        // blocks kb_task..+3 and kb_task+4..+7 are 4 consecutive bytes of two atoms
+        const uint32_t b = row[u] / rows_per_b, r = row[u] - b * rows_per_b;
+        if (full_task) {
+          if (valid[u] && (lane & 15) == 0)
+            *reinterpret_cast<uint32_t*>(s + sf_packed_offset(b, r, kb[u], RT, KT)) = word;
+        } else if (valid[u] && part == 0) {
+          s[sf_packed_offset(b, r, kb[u], RT, KT)] = static_cast<uint8_t>(sbyte);
+        }
+      } else {
+        const uint32_t hi_word = __shfl_sync(0xFFFFFFFFu, word, 16);
+        const int64_t off = static_cast<int64_t>(row[u]) * KB + kb_task;
+        if (full_task && (off & 7) == 0) {
+          if (valid[u] && lane == 0) *reinterpret_cast<uint2*>(s + off) = make_uint2(word, hi_word);
+        } else if (valid[u] && part == 0) {
+          s[static_cast<int64_t>(row[u]) * KB + kb[u]] = static_cast<uint8_t>(sbyte);
         }
       }
     }
@@ -146,19 +171,32 @@ int grid_for(int64_t work_items, int threads, int sms, int per_sm) {
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
                             bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
                             cudaStream_t stream) {
-  const int64_t nblocks = rows * (K / 32);
-  if (nblocks == 0) return cudaSuccess;
-  const int64_t threads_needed = (nblocks + kQuantUnroll - 1) / kQuantUnroll * 4;
-  const int grid = grid_for(threads_needed, kQuantThreads, sms, 8);
-  const int64_t KB = K / 32;
-  const int64_t RT = ceil_div(rows_per_b, kAtomRows), KT = ceil_div(K, kTileK);
   (void)B;
+  const int64_t KB = K / 32;
+  const int64_t tasks_per_row = ceil_div(KB, 8);
+  const int64_t ntasks = rows * tasks_per_row;
+  if (ntasks == 0) return cudaSuccess;
+  if (ntasks > 0x7FFFFFFFll || KB > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  static int per_sm[2] = {0, 0};
+  int& occ = per_sm[packed_scales ? 1 : 0];
+  if (occ == 0) {
+    cudaError_t e = packed_scales
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<true>, kQuantThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<false>, kQuantThreads, 0);
+    if (e != cudaSuccess || occ < 1) occ = 1;
+  }
+  const int64_t warps_needed = ceil_div(ntasks, kQuantUnroll);
+  const int grid = grid_for(warps_needed * 32, kQuantThreads, sms, occ);
+  const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
+  const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
   if (packed_scales)
     quantize_kernel<true><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), nblocks, KB, q, s, rows_per_b, RT, KT);
+        static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
+        static_cast<uint32_t>(ntasks), q, s, static_cast<uint32_t>(rows_per_b), RT, KT);
   else
     quantize_kernel<false><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), nblocks, KB, q, s, rows_per_b, RT, KT);
+        static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
+        static_cast<uint32_t>(ntasks), q, s, static_cast<uint32_t>(rows_per_b), RT, KT);
   return cudaGetLastError();
 }
 
