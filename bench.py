@@ -309,6 +309,7 @@ def run_ours(args):
     ops.check()
 
     decode = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 500))
+    others = _other_workloads(ops, dev, flush, stream, steps=min(max(n, 10), 100))
 
     line = None
     if rank == 0:
@@ -335,6 +336,7 @@ def run_ours(args):
                         "gemm_us": gemm_ms * 1e3, "gemm_tflops": gemm_tflops,
                         "linear_call_us": lin_ms * 1e3},
             "decode_hbm": decode,
+            "other_workloads": others,
             "cpu_baseline": {"value": cpu_rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": f"16 rows x 1024 output columns x K={K}, "
                                        f"{cpu_reps} calls in {cpu_s:.1f} s (fp64 numpy, 1 thread)"},
@@ -353,36 +355,110 @@ def run_ours(args):
 
 
 def _decode_sweep(ops, dev, flush, stream, steps):
-    """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the whole layer."""
+    """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the layer.
+
+    Steady state of a decode loop: a CUDA graph of R back-to-back calls, each on
+    its own copy of the weights (R copies together exceed twice the L2, so every
+    call reads its weights from HBM), replayed `steps` times; per-call time =
+    graph time / R.  Also reported: one call alone after an L2 flush ("cold"),
+    which includes the launch and the SM reconfiguration after the flush.
+    """
     p = synth.decode(64)
     w = _dev_bf16(p.w[0], dev)
     wq, ws = ops.quantize(w)
-    pw = ops.process_weights(wq, ws)
+    base = ops.process_weights(wq, ws)
     bias = _dev_bf16(p.bias, dev)
     del w, wq, ws
+    per_copy = base.w_packed.numel() + base.sf_packed.numel()
+    R = int(np.ceil(2 * 129e6 / per_copy)) + 1
+    pws = [base] + [ops.PackedWeights(base.w_packed.clone(), base.sf_packed.clone(), base.B, base.N,
+                                      base.K, base.batched) for _ in range(R - 1)]
     peaks, _ = _peaks()
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
-    res = {}
+    res = {"weight_copies": R, "timing": "CUDA graph of back-to-back calls over rotating weight copies"}
+    reps = max(3, min(steps, 200))
+    side = torch.cuda.Stream()
     for M in (1, 4, 16, 64):
         x = _dev_bf16(p.x[0, :M], dev)
         out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
-        for _ in range(5):
+        for pw in pws:                                   # warm-up outside capture
             ops.linear(x, pw, bias, out=out, workspace=wsb)
-            flush.zero_()
-        evs = []
-        for _ in range(steps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            ops.linear(x, pw, bias, out=out, workspace=wsb)
-            b.record(stream)
-            flush.zero_()
-            evs.append((a, b))
         torch.cuda.synchronize()
-        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for pw in pws:
+                ops.linear(x, pw, bias, out=out, workspace=wsb)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * R)
+        cold = _time_steps(lambda: ops.linear(x, base, bias, out=out, workspace=wsb), flush, stream,
+                           min(steps, 50))
         nbytes = p.N * p.K + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N + 2 * p.N
         res[f"M{M}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
-                        "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm}
+                        "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "cold_us": cold,
+                        "bytes_per_call": nbytes}
+        del g
+    ops.check()
+    return res
+
+
+def _time_steps(fn, flush, stream, steps):
+    for _ in range(3):
+        fn()
+        flush.zero_()
+    evs = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        flush.zero_()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+
+def _other_workloads(ops, dev, flush, stream, steps):
+    """The pre-quantised prefill (MLP-down) and the batched workload, each
+    through mxfp8_linear, against the roofline that binds it."""
+    peaks, _ = _peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    fp8 = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) * FP8_PER_BF16
+    res = {}
+    # prefill MLP-down, x handed over pre-quantised (row-major scales)
+    p = synth.prefill_down()
+    x_q, x_s = ops.quantize(_dev_bf16(p.x[0], dev))
+    p.x = None
+    wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
+    pw = ops.process_weights(wq, ws)
+    del wq, ws
+    out = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev)
+    wsb = torch.empty(ops.workspace_size(1, p.M, p.N, p.K, True), dtype=torch.uint8, device=dev)
+    us = _time_steps(lambda: ops.linear(x_q, pw, x_scale=x_s, out=out, workspace=wsb), flush, stream, steps)
+    tf = p.flops / (us * 1e-6) / 1e12
+    res["prefill_down_prequantized_M8192_N4096_K14336"] = {
+        "us": us, "tflops": tf, "fp8_peak_frac": tf / fp8, "bound": "tensor"}
+    del x_q, x_s, pw, out, wsb
+    # batched: 16 x (512 x 512 x 7168), bf16 x quantised in the call
+    p = synth.bmm()
+    x = _dev_bf16(p.x, dev)
+    wq, ws = ops.quantize(_dev_bf16(p.w, dev))
+    pw = ops.process_weights(wq, ws)
+    out = torch.empty((p.B, p.M, p.N), dtype=torch.bfloat16, device=dev)
+    wsb = torch.empty(ops.workspace_size(p.B, p.M, p.N, p.K, False), dtype=torch.uint8, device=dev)
+    us = _time_steps(lambda: ops.linear(x, pw, out=out, workspace=wsb), flush, stream, steps)
+    nbytes = p.B * (p.M * p.K * 2 + p.N * p.K + p.N * p.K // 32 + p.M * p.N * 2)
+    res["bmm_B16_M512_N512_K7168"] = {
+        "us": us, "tflops": p.flops / (us * 1e-6) / 1e12, "gbs": nbytes / (us * 1e-6) / 1e9,
+        "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm (x bf16 read once)"}
     ops.check()
     return res
 

@@ -73,7 +73,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kSmallM = 64;  // largest M the fused small-M path serves
+constexpr int kSmallM = mx::kDecodeMaxM;  // largest M the fused small-M path serves
 
 struct WsLayout {
   int64_t xq_off, xq_bytes, sfa_off, sfa_bytes, total;
@@ -235,8 +235,16 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
   if (st != MXFP8_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  if (path == 1) return fail(MXFP8_ERR_UNSUPPORTED, "the small-M fused path is not built yet");
-  (void)kSmallM;
+  const bool small_ok = have_x && B == 1 && M <= kSmallM;
+  if (path == 1 && !small_ok)
+    return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs bf16 x, B == 1 and M <= %d", kSmallM);
+  if (path == 1 || (path == 0 && small_ok)) {
+    mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K};
+    const char* msg = "";
+    cudaError_t e = mx::launch_gemm_decode(p, sms, s, &msg);
+    if (e != cudaSuccess) return cuda_fail(e, msg);
+    return MXFP8_OK;
+  }
 
   const WsLayout ws = prefill_workspace(B, M, K, have_q);
   if (static_cast<int64_t>(workspace_bytes) < ws.total)
@@ -328,12 +336,13 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
 mxfp8_status mxfp8_check(mxfp8_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  unsigned int s1 = 0, s2 = 0, s3 = 0;
+  unsigned int s1 = 0, s2 = 0, s3 = 0, s4 = 0;
   if ((e = mx::take_status_quantize(&s1)) != cudaSuccess ||
       (e = mx::take_status_gemm(&s2)) != cudaSuccess ||
-      (e = mx::take_status_debug(&s3)) != cudaSuccess)
+      (e = mx::take_status_decode(&s3)) != cudaSuccess ||
+      (e = mx::take_status_debug(&s4)) != cudaSuccess)
     return cuda_fail(e, "status word read");
-  if ((s1 | s2 | s3) & 1u) return fail(MXFP8_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
+  if ((s1 | s2 | s3 | s4) & 1u) return fail(MXFP8_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
   return MXFP8_OK;
 }
 

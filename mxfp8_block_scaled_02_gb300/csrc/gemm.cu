@@ -7,17 +7,24 @@
 // bmm_batch_size" as an extra grid dimension.
 //
 // One persistent CTA per SM walks 128 x BN output tiles.  Warp roles:
-//   warp 0      TMA producer: A / W tiles (128-byte swizzle) and scale atoms
-//               into a STAGES-deep shared-memory ring;
-//   warp 1      allocates tensor memory; one lane issues tcgen05.cp (scales to
-//               TMEM) and tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 per
-//               instruction, 4 per 128-wide K tile, scale byte selected by the
-//               instruction descriptor's scale-factor id);
-//   warps 2..9  epilogue: two warps per 32-lane TMEM quarter, each copies its
-//               half of the fp32 accumulator row (BN/2 columns) into registers,
-//               hands the accumulator back to the MMA warp at once, then adds
-//               the bias, rounds to bf16 and stores while the next tile's
-//               main loop already runs.
+//   warp 0       TMA producer: A / W tiles (128-byte swizzle) and scale atoms
+//                into a STAGES-deep shared-memory ring;
+//   warp 1       allocates tensor memory; one lane issues tcgen05.mma
+//                kind::mxf8f6f4 block_scale (K = 32 per instruction, 4 per
+//                128-wide K tile, the scale byte picked by the instruction
+//                descriptor's scale-factor id);
+//   warps 2..5   scale-factor writers, one per 32-lane TMEM quarter: each lane
+//                moves one 16-byte line of the stage's scale atoms from shared
+//                memory into its TMEM lane with tcgen05.st (every quarter gets
+//                the same lines).  Doing this with warps rather than tcgen05.cp
+//                keeps the copies off the tensor pipe, which runs MMAs and
+//                copies in order;
+//   warps 6..13  epilogue, two warps per TMEM quarter, each BN/2 columns: copy
+//                the fp32 accumulator out of TMEM 32 columns at a time, add the
+//                bias and round to bf16 at once, hand the accumulator back to
+//                the MMA warp, then write the bf16 rows through a 2 KB shared
+//                staging buffer with TMA bulk-tensor stores (which also clip
+//                the M / N edges), while the next tile's main loop runs.
 // Every wait is bounded (mx_ptx.cuh); on expiry the roles stop, the kernel
 // drains its own in-flight copies and frees its tensor memory.
 #include <cuda_bf16.h>
@@ -44,12 +51,19 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFA_BYTES = kAtomBytes;
   static constexpr int SFB_BYTES = NB_ATOMS * kAtomBytes;
+  static constexpr int SF_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue thread
+  static constexpr int STAGE_OUT = 32 * 32 * 2;          // one 32 x 32 bf16 box per epilogue warp
+  static constexpr int THREADS = 64 + SF_WARPS * 32 + EPI_THREADS;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2;
+  static constexpr int OFF_OUT = OFF_SFB + STAGES * SFB_BYTES;
+  static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * STAGE_OUT;
+  static constexpr int NUM_BARS = 3 * STAGES + 2;  // full, sf_ready, empty per stage; acc_full/empty
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -59,20 +73,16 @@ struct Cfg {
   static constexpr int T_SFB = T_SFA + STAGES * 4;
   static constexpr int T_END = T_SFB + STAGES * NB_ATOMS * 4;
   static constexpr int TMEM_COLS = T_END <= 256 ? 256 : 512;
-  static constexpr int EPI_WARPS = 8;
-  static constexpr int EPI_THREADS = EPI_WARPS * 32;
-  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue thread
-  static constexpr int THREADS = 64 + EPI_THREADS;
   static_assert(T_END <= 512, "tensor memory overflow");
   static_assert(SMEM_ALLOC <= 232448, "shared memory overflow");
   static_assert(BN % 128 == 0 && BN <= 256, "BN");
+  static_assert(EPI_COLS % 32 == 0, "epilogue chunks");
 };
 
 struct Args {
   const uint8_t* sfa;
   const uint8_t* sfb;
   const __nv_bfloat16* bias;
-  __nv_bfloat16* out;
   int B, M, N, K;
   int MT, NT, KT;  // output tiles along M and N, K tiles
   int RTA, RTB;    // 128-row atom tiles of A and of W
@@ -90,11 +100,12 @@ __device__ __forceinline__ void tile_coords(int tile, const Args& a, int& b, int
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const Args args) {
+                     const __grid_constant__ CUtensorMap tmOut, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + C::STAGES;
+  uint64_t* sf_ready = full + C::STAGES;
+  uint64_t* empty = sf_ready + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -106,6 +117,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&sf_ready[s], C::SF_WARPS * 32);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -114,6 +126,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -182,22 +195,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < args.KT; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          // sf_ready implies the stage's data landed (the writers waited on full)
+          if (!mbar_wait(&sf_ready[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + C::OFF_A + stage * C::A_BYTES);
-          const uint32_t sb = smem_u32(smem + C::OFF_B + stage * C::B_BYTES);
-          const uint32_t ssfa = smem_u32(smem + C::OFF_SFA + stage * C::SFA_BYTES);
-          const uint32_t ssfb = smem_u32(smem + C::OFF_SFB + stage * C::SFB_BYTES);
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_B + stage * C::B_BYTES));
           const uint32_t t_sfa = tmem + C::T_SFA + stage * 4;
           const uint32_t t_sfb = tmem + C::T_SFB + stage * C::NB_ATOMS * 4;
-          tc_cp_sf(t_sfa, sdesc_sf(ssfa));
-#pragma unroll
-          for (int j = 0; j < C::NB_ATOMS; ++j) tc_cp_sf(t_sfb + 4 * j, sdesc_sf(ssfb + j * kAtomBytes));
-          const uint64_t ad = sdesc_kmajor_sw128(sa);
-          const uint64_t bd = sdesc_kmajor_sw128(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             // advance 32 bytes along K inside the 128-byte swizzle row
@@ -217,57 +224,107 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) __nanosleep(200000);  // let issued tensor-core work retire
     }
     __syncwarp();
+  } else if (warp < 2 + C::SF_WARPS) {
+    // ------------------------------------------------------------ scale-factor writers
+    // Atom line `lane` holds rows {lane, lane+32, lane+64, lane+96} x 4 blocks;
+    // the MMA reads it from every 32-lane quarter, so each quarter gets a copy.
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
+      bool ok = true;
+      for (int kt = 0; kt < args.KT; ++kt) {
+        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint4 va = *reinterpret_cast<const uint4*>(smem + C::OFF_SFA + stage * C::SFA_BYTES + lane * 16);
+        tmem_st_32x32b_x4(lane_base + C::T_SFA + stage * 4, va.x, va.y, va.z, va.w);
+#pragma unroll
+        for (int j = 0; j < C::NB_ATOMS; ++j) {
+          const uint4 vb = *reinterpret_cast<const uint4*>(smem + C::OFF_SFB + stage * C::SFB_BYTES +
+                                                           j * kAtomBytes + lane * 16);
+          tmem_st_32x32b_x4(lane_base + C::T_SFB + (stage * C::NB_ATOMS + j) * 4, vb.x, vb.y, vb.z, vb.w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sf_ready[stage]);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2 - C::SF_WARPS;     // 0 .. EPI_WARPS-1
     const int quad = warp & 3;                 // TMEM lane quarter this warp may access
-    const int col0 = ((warp - 2) >> 2) * C::EPI_COLS;
-    const int row = quad * 32 + lane;
+    const int col0 = (ew >> 2) * C::EPI_COLS;
+    uint8_t* stage_out = smem + C::OFF_OUT + ew * C::STAGE_OUT;
     uint32_t acc_phase = 0;
+    bool pending = false;  // lane 0: a bulk store of this warp may still read stage_out
     for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
       int b, mt, nt;
       tile_coords(tile, args, b, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
-      uint32_t r[C::EPI_COLS];
+      // accumulator -> registers as bf16 (bias added in fp32, one rounding)
+      uint32_t packed[C::EPI_COLS / 2];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + col0;
 #pragma unroll
-      for (int c = 0; c < C::EPI_COLS / 32; ++c)
-        tmem_ld_32x32b_x32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-      tmem_ld_wait();
+      for (int c = 0; c < C::EPI_COLS / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int n0 = nt * C::BN + col0 + c * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float bv[8];
+          const int n = n0 + 8 * g;
+          if (args.bias != nullptr && n < args.N) {
+            const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
+            const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              bv[2 * i] = __uint_as_float(bw[i] << 16);
+              bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bv[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            packed[c * 16 + g * 4 + i] = pack_bf16x2(__uint_as_float(r[8 * g + 2 * i]) + bv[2 * i],
+                                                     __uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
+        }
+      }
       tc_fence_before();
       mbar_arrive(acc_empty);                  // accumulator free for the next tile
       acc_phase ^= 1u;
 
-      const int m = mt * BM + row;
-      if (m < args.M) {
-        __nv_bfloat16* orow = args.out + (static_cast<int64_t>(b) * args.M + m) * args.N;
+      // registers -> 32 x 32 staging box -> TMA store (rows/columns past M, N are clipped)
 #pragma unroll
-        for (int g = 0; g < C::EPI_COLS / 8; ++g) {
-          const int n = nt * C::BN + col0 + 8 * g;
-          if (n < args.N) {
-            float bv[8];
-            if (args.bias != nullptr) {
-              const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
-              const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+      for (int c = 0; c < C::EPI_COLS / 32; ++c) {
+        if (lane == 0 && pending) bulk_wait_group_read0();
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 64);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                bv[2 * i] = __uint_as_float(bw[i] << 16);
-                bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) bv[i] = 0.f;
-            }
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[8 * g + 0]) + bv[0], __uint_as_float(r[8 * g + 1]) + bv[1]);
-            o.y = pack_bf16x2(__uint_as_float(r[8 * g + 2]) + bv[2], __uint_as_float(r[8 * g + 3]) + bv[3]);
-            o.z = pack_bf16x2(__uint_as_float(r[8 * g + 4]) + bv[4], __uint_as_float(r[8 * g + 5]) + bv[5]);
-            o.w = pack_bf16x2(__uint_as_float(r[8 * g + 6]) + bv[6], __uint_as_float(r[8 * g + 7]) + bv[7]);
-            *reinterpret_cast<uint4*>(orow + n) = o;
-          }
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(packed[c * 16 + 4 * q], packed[c * 16 + 4 * q + 1], packed[c * 16 + 4 * q + 2],
+                              packed[c * 16 + 4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmOut, stage_out, nt * C::BN + col0 + c * 32, mt * BM + quad * 32, b);
+          bulk_commit_group();
+          pending = true;
         }
       }
     }
+    if (lane == 0 && pending) bulk_wait_group0();
+    __syncwarp();
   }
 
   __syncthreads();
@@ -279,8 +336,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
 using PrefillCfg = Cfg<256, 4>;
 
-cudaError_t make_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows, int64_t K,
-                     int box_rows, const char** msg) {
+// bf16 [B][M][N] output, box {32 columns, 32 rows, 1}, no swizzle.
+cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, int64_t N, const char** msg) {
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) {
+    *msg = "cuTensorMapEncodeTiled is not available from the driver";
+    return cudaErrorNotSupported;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N * 2), static_cast<cuuint64_t>(M * N * 2)};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *msg = "cuTensorMapEncodeTiled rejected the output";
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+// 3-D map over [B][rows][K] bytes, box {128, box_rows, 1}, 128-byte swizzle,
+// zero fill outside the tensor.
+cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
+                             int64_t K, int box_rows, const char** msg) {
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) {
     *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -301,8 +384,6 @@ cudaError_t make_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t r
   return cudaSuccess;
 }
 
-}  // namespace
-
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
   using C = PrefillCfg;
   static bool attr_set[64] = {};
@@ -317,17 +398,18 @@ cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stre
     }
     attr_set[dev] = true;
   }
-  CUtensorMap ma, mb;
-  cudaError_t e = make_map(&ma, p.a, p.B, p.M, p.K, BM, msg);
+  CUtensorMap ma, mb, mo;
+  cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, BM, msg);
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, p.w, p.B, p.N, p.K, C::BN, msg);
+  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, C::BN, msg);
+  if (e != cudaSuccess) return e;
+  e = make_output_map(&mo, p.out, p.B, p.M, p.N, msg);
   if (e != cudaSuccess) return e;
 
   Args a;
   a.sfa = p.sfa;
   a.sfb = p.sfb;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
-  a.out = static_cast<__nv_bfloat16*>(p.out);
   a.B = static_cast<int>(p.B);
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);
@@ -339,7 +421,7 @@ cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stre
   a.RTB = static_cast<int>(ceil_div(p.N, kAtomRows));
   a.total_tiles = a.B * a.MT * a.NT;
   const int grid = a.total_tiles < sms ? a.total_tiles : sms;
-  gemm_mxf8_kernel<C><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(ma, mb, a);
+  gemm_mxf8_kernel<C><<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(ma, mb, mo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) *msg = "GEMM launch failed";
   return e;

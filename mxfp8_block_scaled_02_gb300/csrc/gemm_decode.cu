@@ -1,0 +1,428 @@
+// gemm_decode.cu - the small-M (decode) path of the MXFP8 linear layer.
+//
+// out[m, n] = bf16( sum_k deq(x)[m, k] * deq(w)[n, k] + bias[n] ), M <= 64,
+// with x bf16 quantised to MXFP8 inside the kernel: the block-scaled product
+// and bias add of "AiterFlyDSLMxfp8LinearKernel.apply_weights" (aiter_flydsl
+// page), with its mxfp8_e4m3_quantize step fused into the GEMM producer.
+//
+// At small M the layer is bound by reading the weights once from HBM, so:
+//   * the weights are the MMA's A operand (M = 128 weight rows per CTA) and the
+//     tokens its B operand (N = 16, 32 or 64 >= M), so no MMA rows are wasted
+//     on padding tokens;
+//   * K is split over a cluster of S CTAs (S in {1, 2, 4, 8}, the largest
+//     whose clusters all fit on the GPU at once); each CTA streams its
+//     128 x K/S weight slice through a TMA ring (at N = K = 4096 and M <= 16:
+//     S = 8, 4 K tiles per CTA, the whole slice in flight from the start);
+//   * warps 2..9 read x (bf16, from L2) and quantise it with the same device
+//     function as the standalone quantize kernel, writing E4M3 codes straight
+//     into the 128-byte-swizzled operand tile and the scales into the
+//     scale-factor atom.  They work on groups of K tiles and issue the next
+//     group's loads before quantising the current one, so the latency of x is
+//     paid about once;
+//   * the S fp32 partial tiles meet in distributed shared memory: CTA r owns
+//     weight rows [r*128/S, (r+1)*128/S); every CTA stores its partial for
+//     those rows straight into the owner's receive buffer (remote shared-memory
+//     stores), then one cluster barrier, then each owner sums its S partials
+//     in the fixed order 0..S-1 (deterministic), adds the bias and stores bf16;
+//   * programmatic dependent launch: the weight loads, which depend on nothing
+//     the previous kernel in the stream writes, start before
+//     griddepcontrol.wait; reading x and writing out come after it, so
+//     consecutive layers overlap one's tail with the next one's weight stream.
+// Two shapes of the kernel: up to 16 tokens (4-stage ring, ~86 KB of shared
+// memory, two CTAs per SM so that the next call's CTAs fit beside this one's)
+// and up to 64 tokens (6-stage ring, one CTA per SM).
+// Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
+// and MMA issuer, 2..9 = activation quantiser, then (2..5) TMEM -> remote
+// shared memory and (2..9) the reduction.
+// Every mbarrier wait is bounded; the cluster barrier is reached on every
+// path, also after an expired wait.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mx_kernels.h"
+#include "mx_layout.cuh"
+#include "mx_ptx.cuh"
+#include "mx_quant.cuh"
+
+namespace mx {
+
+namespace {
+
+constexpr int kRows = 128;  // weight rows per CTA = MMA M
+constexpr int kTK = 128;    // K elements per stage
+constexpr int QTHREADS = 256;  // warps 2..9
+constexpr int THREADS = 64 + QTHREADS;
+constexpr int kWBytes = kRows * kTK;  // 16 KB
+
+template <int MAXTOK_, int STAGES_, int QLOADS_, int MINB_>
+struct DCfg {
+  static constexpr int MAXTOK = MAXTOK_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int QLOADS = QLOADS_;  // 16-byte x loads per quantiser thread per group
+  static constexpr int MINB = MINB_;      // CTAs per SM the kernel is built for
+  static constexpr int XBYTES = MAXTOK * kTK;
+  static constexpr int OFF_W = 0;
+  static constexpr int OFF_X = OFF_W + STAGES * kWBytes;
+  static constexpr int OFF_SFW = OFF_X + STAGES * XBYTES;
+  static constexpr int OFF_SFX = OFF_SFW + STAGES * kAtomBytes;
+  static constexpr int OFF_RECV = OFF_SFX + STAGES * kAtomBytes;  // [S][n_mma][128/S] fp32
+  static constexpr int RECV_BYTES = MAXTOK * kRows * 4;
+  static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
+  static constexpr int NUM_BARS = 3 * STAGES + 1;  // full_w, full_x, empty per stage; acc_full
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+  static constexpr int T_ACC = 0;  // MAXTOK fp32 columns
+  static constexpr int T_SFW = MAXTOK;
+  static constexpr int T_SFX = T_SFW + 4 * STAGES;
+  static constexpr int T_END = T_SFX + 4 * STAGES;
+  static constexpr int TMEM_COLS = T_END <= 32 ? 32 : (T_END <= 64 ? 64 : 128);
+  static_assert(T_END <= 128, "tensor memory");
+  static_assert(MINB * SMEM_ALLOC <= 232448, "shared memory");
+  static_assert(QTHREADS % kRows == 0, "each reduction thread owns one output column");
+};
+
+using SmallCfg = DCfg<16, 4, 4, 2>;
+using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 1>;
+
+struct Args {
+  const uint4* x;  // bf16 [M, K] as 16-byte chunks
+  const uint8_t* sfw;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  int M, N, K;
+  int n_mma;   // MMA N: 16, 32 or 64 (>= M)
+  int KT;      // K / 128
+  int RTW;     // 128-row atom tiles of the weights
+  int splits;  // cluster size S
+};
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class C>
+__global__ void __launch_bounds__(THREADS, C::MINB)
+    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full_x = full_w + C::STAGES;
+  uint64_t* empty = full_x + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int tile = blockIdx.x / a.splits;
+  const int kt0 = static_cast<int>(static_cast<int64_t>(rank) * a.KT / a.splits);
+  const int kt1 = static_cast<int>(static_cast<int64_t>(rank + 1) * a.KT / a.splits);
+  const int nk = kt1 - kt0;  // >= 1 because splits <= KT
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_w[s], 1);
+      mbar_init(&full_x[s], QTHREADS);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ weight producer (TMA)
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int st = i % C::STAGES;
+        const uint32_t ph = (i / C::STAGES) & 1;
+        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(&full_w[st], kWBytes + kAtomBytes);
+        tma_load_3d(smem + C::OFF_W + st * kWBytes, &tmW, &full_w[st], (kt0 + i) * kTK, tile * kRows, 0);
+        bulk_load(smem + C::OFF_SFW + st * kAtomBytes,
+                  a.sfw + (static_cast<int64_t>(kt0 + i) * a.RTW + tile) * kAtomBytes, kAtomBytes,
+                  &full_w[st]);
+        ++issued;
+        if (i + 1 == min(nk, C::STAGES)) launch_dependents();  // the next kernel may start loading
+      }
+      if (*abort_flag) {
+        for (int s = 0; s < C::STAGES && s < issued; ++s) {
+          const int last = ((issued - 1 - s) / C::STAGES) * C::STAGES + s;
+          mbar_wait(&full_w[s], static_cast<uint32_t>((last / C::STAGES) & 1), nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_mxf8(kRows, a.n_mma);
+      bool ok = true;
+      for (int i = 0; i < nk && ok; ++i) {
+        const int st = i % C::STAGES;
+        const uint32_t ph = (i / C::STAGES) & 1;
+        if (!mbar_wait(&full_w[st], ph, abort_flag) || !mbar_wait(&full_x[st], ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_sfw = tmem + C::T_SFW + st * 4;
+        const uint32_t t_sfx = tmem + C::T_SFX + st * 4;
+        tc_cp_sf(t_sfw, sdesc_sf(smem_u32(smem + C::OFF_SFW + st * kAtomBytes)));
+        tc_cp_sf(t_sfx, sdesc_sf(smem_u32(smem + C::OFF_SFX + st * kAtomBytes)));
+        const uint64_t ad = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_W + st * kWBytes));
+        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_X + st * C::XBYTES));
+#pragma unroll
+        for (int kk = 0; kk < kTK / 32; ++kk)
+          tc_mma_mxf8(tmem + C::T_ACC, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk), t_sfw,
+                      t_sfx, (i | kk) != 0);
+        tc_commit(&empty[st]);
+      }
+      if (ok) tc_commit(acc_full);
+      else __nanosleep(200000);  // let issued tensor-core work retire
+    }
+    __syncwarp();
+  } else {
+    // x is written by the previous kernel in the stream: wait for it to finish.
+    grid_dependency_wait();
+    // ------------------------------------------------ activation quantiser
+    // A task is one 16-byte chunk (8 bf16) of x: k tile i, row r < n_mma,
+    // chunk qd < 16 of the row's 128 values.  One group = G k tiles =
+    // G * n_mma * 16 tasks, at most QLOADS per thread.
+    const int t = threadIdx.x - 64;
+    const int pt_shift = 31 - __clz(a.n_mma * 16);  // n_mma is a power of two
+    const int per_tile = 1 << pt_shift;
+    // A group's ring slots must all be free at once while the MMA still owns
+    // the others, so a group spans at most half the ring.
+    const int G = max(1, min(C::STAGES / 2, (QTHREADS * C::QLOADS) >> pt_shift));
+    const int per_group = G * per_tile;  // a multiple of QTHREADS: whole warps
+    auto load_group = [&](int g, uint4 (&dst)[C::QLOADS]) {
+#pragma unroll
+      for (int j = 0; j < C::QLOADS; ++j) {
+        const int task = t + j * QTHREADS;
+        const int i = g * G + (task >> pt_shift);
+        const int rem = task & (per_tile - 1);
+        const int row = rem >> 4, qd = rem & 15;
+        dst[j] = (task < per_group && i < nk && row < a.M)
+                     ? __ldg(a.x + (static_cast<int64_t>(row) * a.K + (kt0 + i) * kTK) / 8 + qd)
+                     : make_uint4(0, 0, 0, 0);
+      }
+    };
+    // Wait for the group's ring slots, quantise it into them, signal the MMA.
+    auto quantize_group = [&](int g, const uint4 (&cur)[C::QLOADS]) -> bool {
+      for (int i = g * G; i < min(nk, (g + 1) * G); ++i)
+        if (!mbar_wait(&empty[i % C::STAGES], ((i / C::STAGES) & 1) ^ 1u, abort_flag)) return false;
+#pragma unroll
+      for (int j = 0; j < C::QLOADS; ++j) {
+        const int task = t + j * QTHREADS;
+        const int i = g * G + (task >> pt_shift);
+        const int rem = task & (per_tile - 1);
+        const int row = rem >> 4, qd = rem & 15;
+        uint2 codes;
+        const uint32_t sbyte = quantize_quarter_block(cur[j], codes);  // all lanes take part
+        if (task < per_group && i < nk) {
+          const int st = i % C::STAGES;
+          uint8_t* xt = smem + C::OFF_X + st * C::XBYTES;
+          uint8_t* sft = smem + C::OFF_SFX + st * kAtomBytes;
+          // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+          const int chunk = qd >> 1;
+          *reinterpret_cast<uint2*>(xt + row * 128 + ((chunk ^ (row & 7)) << 4) + (qd & 1) * 8) = codes;
+          if ((qd & 3) == 0)
+            sft[(row & 31) * 16 + (row >> 5) * 4 + (qd >> 2)] = static_cast<uint8_t>(sbyte);
+        }
+      }
+      fence_proxy_async_smem();
+      for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::STAGES]);
+      return true;
+    };
+    const int ngroups = (nk + G - 1) / G;
+    uint4 buf0[C::QLOADS], buf1[C::QLOADS];  // two register sets: load one group ahead
+    load_group(0, buf0);
+    for (int g = 0; g < ngroups; g += 2) {
+      if (g + 1 < ngroups) load_group(g + 1, buf1);
+      if (!quantize_group(g, buf0)) break;
+      if (g + 1 >= ngroups) break;
+      if (g + 2 < ngroups) load_group(g + 2, buf0);
+      if (!quantize_group(g + 1, buf1)) break;
+    }
+
+    // ------------------------------------------------ epilogue: TMEM -> owner's receive buffer
+    if (warp < 6 && mbar_wait(acc_full, 0, abort_flag)) {
+      tc_fence_after();
+      const int quad = warp & 3;
+      const int wrow = quad * 32 + lane;  // weight row within the tile = TMEM lane
+      const int per = kRows / a.splits;
+      const uint32_t owner = static_cast<uint32_t>(wrow / per);
+      const int nl = wrow - static_cast<int>(owner) * per;
+      const uint32_t dst = map_shared_rank(smem_u32(smem + C::OFF_RECV), owner) +
+                           static_cast<uint32_t>(((rank * a.n_mma) * per + nl) * 4);
+      for (int c = 0; c < a.n_mma; c += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) st_shared_cluster_u32(dst + static_cast<uint32_t>((c + j) * per * 4), r[j]);
+      }
+    }
+  }
+
+  // ------------------------------------------------ split-K reduction (owner sums)
+  tc_fence_before();
+  cluster_sync();  // all partials have landed in their owners' receive buffers
+  if (threadIdx.x >= 64 && !*abort_flag) {
+    const int t = threadIdx.x - 64;
+    const int per = kRows / a.splits;
+    const float* recv = reinterpret_cast<const float*>(smem + C::OFF_RECV);
+    // QTHREADS is a multiple of per, so each thread keeps one output column n
+    const int nl = t % per;
+    const int n = tile * kRows + static_cast<int>(rank) * per + nl;
+    const float bias = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.f;
+    if (n < a.N) {
+#pragma unroll 4
+      for (int m = t / per; m < a.M; m += QTHREADS / per) {
+        float acc = 0.f;
+        for (int s2 = 0; s2 < a.splits; ++s2) acc += recv[(s2 * a.n_mma + m) * per + nl];
+        a.out[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc + bias);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <class C>
+cudaError_t prepare_cfg(const char** msg) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) {
+      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      return e;
+    }
+    attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// Clusters of `splits` CTAs of this kernel that fit on the GPU at once (asked
+// of the driver once per device and cluster size).
+template <class C>
+int max_active_clusters(int splits) {
+  static int cache[64][4] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int slot = splits == 8 ? 3 : (splits == 4 ? 2 : (splits == 2 ? 1 : 0));
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev][slot] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<C>, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();  // clear the sticky-free error state of the failed query
+      n = -1;
+    }
+    cache[dev][slot] = n;
+  }
+  return cache[dev][slot];
+}
+
+template <class C>
+cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStream_t stream,
+                       const char** msg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<C>, mw, a);
+  if (e != cudaSuccess) *msg = "decode GEMM launch failed";
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg) {
+  CUtensorMap mw;
+  cudaError_t e = make_operand_map(&mw, p.w, 1, p.N, p.K, kRows, msg);
+  if (e != cudaSuccess) return e;
+
+  Args a;
+  a.x = static_cast<const uint4*>(p.x);
+  a.sfw = p.sfw;
+  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.out = static_cast<__nv_bfloat16*>(p.out);
+  a.M = static_cast<int>(p.M);
+  a.N = static_cast<int>(p.N);
+  a.K = static_cast<int>(p.K);
+  a.n_mma = p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64);  // a power of two: shifts in the quantiser
+  a.KT = static_cast<int>(p.K / kTK);
+  a.RTW = static_cast<int>(ceil_div(p.N, kAtomRows));
+  const int tiles = a.RTW;
+  const bool small = a.n_mma <= SmallCfg::MAXTOK;
+  e = small ? prepare_cfg<SmallCfg>(msg) : prepare_cfg<LargeCfg>(msg);
+  if (e != cudaSuccess) return e;
+  // The largest split (at most 8, at most one per K tile) whose clusters all
+  // fit on the GPU at once, so that every CTA streams its weights from the start.
+  const int per_sm = small ? SmallCfg::MINB : LargeCfg::MINB;
+  int splits = 8;
+  while (splits > 1) {
+    const int fit = small ? max_active_clusters<SmallCfg>(splits) : max_active_clusters<LargeCfg>(splits);
+    const bool fits = fit > 0 ? tiles <= fit : tiles * splits <= per_sm * sms;
+    if (splits <= a.KT && fits) break;
+    splits >>= 1;
+  }
+  a.splits = splits;
+  const int grid = tiles * splits;
+  return small ? launch_cfg<SmallCfg>(mw, a, grid, stream, msg)
+               : launch_cfg<LargeCfg>(mw, a, grid, stream, msg);
+}
+
+cudaError_t take_status_decode(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mx

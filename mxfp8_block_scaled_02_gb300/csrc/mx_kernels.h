@@ -32,6 +32,24 @@ struct GemmProblem {
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
 cudaError_t take_status_gemm(unsigned int* out);
+// 3-D TMA map over [B][rows][K] E4M3 bytes, box {128, box_rows, 1}, 128-byte swizzle.
+cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
+                             int64_t K, int box_rows, const char** msg);
+
+// gemm_decode.cu: the small-M path (M <= 64, B = 1, bf16 x): weights on the
+// MMA's M side, activations quantised inside the kernel, split-K across a
+// thread-block cluster with a fixed-order reduction in distributed shared memory.
+struct DecodeProblem {
+  const void* x;     // bf16 [M, K]
+  const uint8_t* w;  // E4M3 [N, K]
+  const uint8_t* sfw;
+  const void* bias;  // bf16 [N] or nullptr
+  void* out;         // bf16 [M, N]
+  int64_t M, N, K;
+};
+constexpr int kDecodeMaxM = 64;
+cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg);
+cudaError_t take_status_decode(unsigned int* out);
 
 // debug.cu
 cudaError_t launch_expire_wait(uint64_t timeout_ns, cudaStream_t stream);

@@ -1,0 +1,55 @@
+// mx_quant.cuh - the MXFP8 quantisation step shared by the standalone
+// quantize kernel and the fused small-M GEMM, so that both produce the same
+// bytes.
+//
+// Rule (OCP MX v1.0, section 6.3, for the "MXFP8 format" of the
+// CompressedTensorsW8A8Mxfp8 page): per 32-element block, e = floor(log2 amax)
+// - 8 clamped to [-127, 127], scale byte e + 127, element E4M3(x / 2^e) with
+// round-to-nearest-even and saturation to +-448; a block holding Inf/NaN gets
+// byte 0xFF and elements 0x7F.  Decided on bf16 bit patterns:
+//   * |x| as an integer is (bits & 0x7FFF): integer order is value order for
+//     non-negative floats, and Inf/NaN are exactly the patterns >= 0x7F80;
+//   * for a finite amax with exponent field E, floor(log2 amax) = E - 127, so
+//     the byte is max(E - 8, 0) (zero and subnormal blocks clamp to 0);
+//   * 2^-e = 2^(127 - byte) is a normal fp32 for byte in [0, 246], and x * 2^-e
+//     is exact in fp32 unless it underflows, which rounds to a signed zero in
+//     E4M3 either way;
+//   * fp32 -> E4M3 is the hardware's cvt.rn.satfinite.e4m3x2.
+#pragma once
+
+#include <stdint.h>
+
+#include "mx_ptx.cuh"
+
+namespace mx {
+
+// Quantise 8 consecutive bf16 values (one 16-byte load) that are one quarter
+// of a 32-element block; the block's four quarters sit in four consecutive
+// lanes (lane % 4 = quarter).  Must be called by all 32 lanes of the warp.
+// Returns the block's scale byte (same in the four lanes) and the 8 codes.
+__device__ __forceinline__ uint32_t quantize_quarter_block(const uint4 v, uint2& codes) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+
+  const bool nonfinite = amax >= 0x7F80u;
+  const uint32_t E = amax >> 7;
+  const uint32_t sbyte = nonfinite ? 0xFFu : (E > 8u ? E - 8u : 0u);
+  const float mul = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);
+
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * mul;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * mul;
+    c[i] = cvt_e4m3x2(lo, hi);
+  }
+  codes = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  if (nonfinite) codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  return sbyte;
+}
+
+}  // namespace mx

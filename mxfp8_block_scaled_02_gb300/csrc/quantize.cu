@@ -1,20 +1,7 @@
 // quantize.cu - dynamic MXFP8 quantisation and the scale-factor repack.
 //
-// Quantisation rule (OCP MX v1.0, section 6.3, for the MXFP8 format of the
-// "CompressedTensorsW8A8Mxfp8" page): per 32-element block along K the scale
-// exponent is floor(log2 amax) - 8, clamped to [-127, 127]; each element is
-// x / 2^e rounded to E4M3, nearest-even, saturating to +-448.
-//
-// Everything is decided on the bf16 bit patterns:
-//   * |x| as an integer is (bits & 0x7FFF); for non-negative floats integer
-//     order is value order, and NaN/Inf are exactly the patterns >= 0x7F80.
-//   * for a finite amax with biased exponent field E (E = 0 for zero and
-//     subnormals) floor(log2 amax) = E - 127, so the scale byte is
-//     max(E - 8, 0); every subnormal or zero block clamps to byte 0.
-//   * 2^-e = 2^(127 - byte) is a normal fp32 for byte in [0, 246], and x * 2^-e
-//     is exact in fp32 unless it underflows, in which case the result rounds
-//     to a signed zero in E4M3 either way.
-//   * the fp32 -> E4M3 rounding is the hardware's cvt.rn.satfinite.e4m3x2.
+// The per-block arithmetic (OCP MX v1.0, section 6.3) lives in mx_quant.cuh,
+// shared with the fused small-M GEMM so that both produce the same bytes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -22,6 +9,7 @@
 #include "mx_kernels.h"
 #include "mx_layout.cuh"
 #include "mx_ptx.cuh"
+#include "mx_quant.cuh"
 
 namespace mx {
 
@@ -61,27 +49,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t amax = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-
-      const bool nonfinite = amax >= 0x7F80u;
-      const uint32_t E = amax >> 7;
-      const uint32_t sbyte = nonfinite ? 0xFFu : (E > 8u ? E - 8u : 0u);
-      const float mul = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);
-
-      uint32_t c[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16) * mul;
-        const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * mul;
-        c[i] = cvt_e4m3x2(lo, hi);
-      }
-      uint2 out = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-      if (nonfinite) out = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      uint2 out;
+      const uint32_t sbyte = quantize_quarter_block(v[u], out);
       const int64_t blk = static_cast<int64_t>(row[u]) * KB + kb[u];
       if (valid[u]) *reinterpret_cast<uint2*>(q + blk * 32 + part * 8) = out;
 

@@ -230,3 +230,76 @@ def test_prefill_down_prequantized_sampled():
 
 def test_bmm_workload():
     _bf16_problem_check(synth.bmm())
+
+
+# ------------------------------------------------------------------ small-M path
+def _bf16_exact_block_input(M, K, seed):
+    """bf16 x whose 32-blocks are +-2^d (d per row and block): quantised exactly."""
+    rng = np.random.default_rng(seed)
+    d = rng.integers(-3, 4, (M, K // 32))
+    sign = rng.choice([-1.0, 1.0], (M, K))
+    return sign * np.repeat(np.ldexp(1.0, d), 32, axis=1)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (4, 256, 512), (16, 136, 1024), (33, 264, 256),
+                                   (64, 128, 4096)])
+def test_small_m_path_exact_block_scales(M, N, K):
+    """x with a distinct power-of-two block scale per (row, block), integer W:
+    exact sums, so the small-M path must equal bf16(oracle) bit for bit."""
+    dev = device()
+    x = _bf16_exact_block_input(M, K, seed=M + K)
+    rng = np.random.default_rng(N)
+    wi = rng.integers(-8, 9, (N, K)).astype(np.float64)
+    wq, ws = oracle.quantize(wi)
+    pw = _pack(wq, ws, dev)
+    out = ops.linear(bf16_to_dev(synth.to_bf16_bits(x), dev), pw, path=1)
+    ops.check()
+    xq, xs = oracle.quantize(x)
+    ref = oracle.linear(xq, xs, wq, ws)
+    got = bf16_bits(out)
+    exp = _exact_bits(ref)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)}/{got.size} mismatches; first {i}: got "
+                             f"{synth.bf16_bits_to_f64(np.array([got[i]]))[0]} ref {ref[i]}")
+
+
+@pytest.mark.parametrize("M,N,K,bias", [(1, 8, 128, True), (3, 136, 256, False),
+                                        (17, 520, 1024, True), (64, 4096, 512, True),
+                                        (48, 1000, 7168, True)])
+def test_small_m_path_against_oracle(M, N, K, bias):
+    p = synth.make_problem("small", 1, M, N, K, seed=M * 7 + N, bias_std=0.1 if bias else None)
+    _bf16_problem_check(p, path=1)
+
+
+def test_small_m_and_large_m_paths_agree():
+    dev = device()
+    p = synth.make_problem("paths", 1, 40, 1024, 2048, seed=77, bias_std=0.1)
+    wq, ws = oracle_weights(p)
+    pw = _pack(wq[0], ws[0], dev)
+    x = bf16_to_dev(p.x[0], dev)
+    bias = bf16_to_dev(p.bias, dev)
+    a = ops.linear(x, pw, bias, path=1)
+    b = ops.linear(x, pw, bias, path=2)
+    ops.check()
+    from _helpers import tolerance_violations
+    bad = tolerance_violations(a.float().cpu().numpy().astype(np.float64),
+                               b.float().cpu().numpy().astype(np.float64))
+    assert not bad.any()
+
+
+def test_small_m_path_refuses_what_it_cannot_do():
+    dev = device()
+    p = synth.make_problem("refuse", 2, 8, 128, 256, seed=5)
+    wq, ws = oracle_weights(p)
+    pw = _pack(wq, ws, dev)
+    with pytest.raises(ops.MxStatusError) as ei:      # batched
+        ops.linear(bf16_to_dev(p.x, dev), pw, path=1)
+    assert ei.value.status == 2
+    big = synth.make_problem("big", 1, 65, 128, 256, seed=6)
+    wq, ws = oracle_weights(big)
+    pw = _pack(wq[0], ws[0], dev)
+    with pytest.raises(ops.MxStatusError):            # M > 64
+        ops.linear(bf16_to_dev(big.x[0], dev), pw, path=1)
+    ops.check()
