@@ -151,9 +151,11 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * mxfp8_linear_path - mxfp8_linear with the kernel path chosen by the caller
  * instead of by M: path 0 = automatic (as mxfp8_linear), 1 = small-M path
  * (quantisation fused into the GEMM, weights on the MMA's M side), 2 = large-M
- * path (separate quantise kernel, then the GEMM).  Both paths compute the same
- * function; this exists so that tests can check each on every shape.
- * Path 1 needs M <= 64 and x_bf16 (else MXFP8_ERR_UNSUPPORTED).
+ * path (separate quantise kernel, then the GEMM with one CTA per 128 x 256
+ * tile), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
+ * cta_group::2; not yet faster, kept selectable and tested).  All paths
+ * compute the same function; this exists so that tests can check each on
+ * every shape.  Path 1 needs M <= 64 and x_bf16 (else MXFP8_ERR_UNSUPPORTED).
  */
 mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
                                const uint8_t* x_scale, int64_t B, int64_t M, int64_t N,

@@ -211,7 +211,7 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
                                const uint8_t* w_packed, const uint8_t* sf_packed,
                                const void* bias_bf16, void* out_bf16, void* workspace,
                                size_t workspace_bytes, mxfp8_stream_t stream) {
-  if (path < 0 || path > 2) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
+  if (path < 0 || path > 3) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
   {
     mxfp8_status ck = check_gemm_args(B, M, N, K);
     if (ck != MXFP8_OK) return ck;
@@ -265,7 +265,7 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
     e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
-  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K};
+  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : 1};
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);
   if (e != cudaSuccess) return cuda_fail(e, msg);
@@ -336,13 +336,14 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
 mxfp8_status mxfp8_check(mxfp8_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  unsigned int s1 = 0, s2 = 0, s3 = 0, s4 = 0;
+  unsigned int s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0;
   if ((e = mx::take_status_quantize(&s1)) != cudaSuccess ||
       (e = mx::take_status_gemm(&s2)) != cudaSuccess ||
       (e = mx::take_status_decode(&s3)) != cudaSuccess ||
-      (e = mx::take_status_debug(&s4)) != cudaSuccess)
+      (e = mx::take_status_pair(&s4)) != cudaSuccess ||
+      (e = mx::take_status_debug(&s5)) != cudaSuccess)
     return cuda_fail(e, "status word read");
-  if ((s1 | s2 | s3 | s4) & 1u) return fail(MXFP8_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
+  if ((s1 | s2 | s3 | s4 | s5) & 1u) return fail(MXFP8_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
   return MXFP8_OK;
 }
 

@@ -8,7 +8,9 @@
 //
 // One persistent CTA per SM walks 128 x BN output tiles.  Warp roles:
 //   warp 0       TMA producer: A / W tiles (128-byte swizzle) and scale atoms
-//                into a STAGES-deep shared-memory ring;
+//                into a STAGES-deep shared-memory ring; the atoms complete on
+//                their own barrier so their trip to TMEM overlaps the
+//                operand load;
 //   warp 1       allocates tensor memory; one lane issues tcgen05.mma
 //                kind::mxf8f6f4 block_scale (K = 32 per instruction, 4 per
 //                128-wide K tile, the scale byte picked by the instruction
@@ -63,7 +65,8 @@ struct Cfg {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_OUT = OFF_SFB + STAGES * SFB_BYTES;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * STAGE_OUT;
-  static constexpr int NUM_BARS = 3 * STAGES + 2;  // full, sf_ready, empty per stage; acc_full/empty
+  // per stage: full (operands), sf_full (scale atoms), sf_ready, empty; then acc_full/empty
+  static constexpr int NUM_BARS = 4 * STAGES + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -104,7 +107,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* sf_ready = full + C::STAGES;
+  uint64_t* sf_full = full + C::STAGES;
+  uint64_t* sf_ready = sf_full + C::STAGES;
   uint64_t* empty = sf_ready + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 1;
@@ -117,11 +121,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&sf_ready[s], C::SF_WARPS * 32);
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_ready[s], C::SF_WARPS);  // one arrive per writer warp
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, C::EPI_THREADS);
+    mbar_init(acc_empty, C::EPI_WARPS);  // one arrive per epilogue warp
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -148,22 +153,25 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int b, mt, nt;
         tile_coords(tile, args, b, mt, nt);
         const int nb_atoms = min(C::NB_ATOMS, args.RTB - nt * C::NB_ATOMS);
-        const uint32_t tx = C::A_BYTES + C::B_BYTES + C::SFA_BYTES + nb_atoms * kAtomBytes;
+        const uint32_t sf_tx = C::SFA_BYTES + nb_atoms * kAtomBytes;
         for (int kt = 0; kt < args.KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], tx);
+          // The scale atoms get their own barrier: they land long before the
+          // operands, so the writers put them in TMEM while the operands load.
+          const int64_t arow = static_cast<int64_t>(b) * args.KT + kt;
+          mbar_arrive_expect_tx(&sf_full[stage], sf_tx);
+          bulk_load(smem + C::OFF_SFA + stage * C::SFA_BYTES,
+                    args.sfa + (arow * args.RTA + mt) * kAtomBytes, C::SFA_BYTES, &sf_full[stage]);
+          bulk_load(smem + C::OFF_SFB + stage * C::SFB_BYTES,
+                    args.sfb + (arow * args.RTB + static_cast<int64_t>(nt) * C::NB_ATOMS) * kAtomBytes,
+                    nb_atoms * kAtomBytes, &sf_full[stage]);
+          mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
           tma_load_3d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kt * BK, mt * BM, b);
           tma_load_3d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kt * BK,
                       nt * C::BN, b);
-          const int64_t arow = static_cast<int64_t>(b) * args.KT + kt;
-          bulk_load(smem + C::OFF_SFA + stage * C::SFA_BYTES,
-                    args.sfa + (arow * args.RTA + mt) * kAtomBytes, C::SFA_BYTES, &full[stage]);
-          bulk_load(smem + C::OFF_SFB + stage * C::SFB_BYTES,
-                    args.sfb + (arow * args.RTB + static_cast<int64_t>(nt) * C::NB_ATOMS) * kAtomBytes,
-                    nb_atoms * kAtomBytes, &full[stage]);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -177,6 +185,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (issued <= s) continue;
           const int64_t last = ((issued - 1 - s) / C::STAGES) * C::STAGES + s;
           mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), nullptr);
+          mbar_wait(&sf_full[s], static_cast<uint32_t>((last / C::STAGES) & 1), nullptr);
         }
       }
     }
@@ -195,8 +204,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tc_fence_after();
         for (int kt = 0; kt < args.KT; ++kt) {
-          // sf_ready implies the stage's data landed (the writers waited on full)
-          if (!mbar_wait(&sf_ready[stage], phase, abort_flag)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&sf_ready[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
       bool ok = true;
       for (int kt = 0; kt < args.KT; ++kt) {
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        if (!mbar_wait(&sf_full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
@@ -248,7 +256,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&sf_ready[stage]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -301,7 +310,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(acc_empty);                  // accumulator free for the next tile
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);   // accumulator free for the next tile
       acc_phase ^= 1u;
 
       // registers -> 32 x 32 staging box -> TMA store (rows/columns past M, N are clipped)
@@ -336,6 +346,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
 using PrefillCfg = Cfg<256, 4>;
 
+}  // namespace
+
 // bf16 [B][M][N] output, box {32 columns, 32 rows, 1}, no swizzle.
 cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, int64_t N, const char** msg) {
   EncodeTiledFn encode = encode_tiled_fn();
@@ -357,8 +369,6 @@ cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, i
   }
   return cudaSuccess;
 }
-
-}  // namespace
 
 // 3-D map over [B][rows][K] bytes, box {128, box_rows, 1}, 128-byte swizzle,
 // zero fill outside the tensor.
@@ -385,6 +395,7 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, i
 }
 
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
+  if (p.tiles == 2) return launch_gemm_pair(p, sms, stream, msg);
   using C = PrefillCfg;
   static bool attr_set[64] = {};
   int dev = 0;

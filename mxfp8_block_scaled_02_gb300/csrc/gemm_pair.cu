@@ -1,0 +1,426 @@
+// gemm_pair.cu - the block-scaled MXFP8 GEMM on CTA pairs (cta_group::2).
+//
+// Same function as gemm.cu (the block-scaled product and bias add of
+// "AiterFlyDSLMxfp8LinearKernel.apply_weights", aiter_flydsl page, batched per
+// "Mxfp8LinearLayerConfig.bmm_batch_size"), for M > 128.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2: CTA r holds rows [128 r, 128 r + 128) of the
+// activation tile and rows [128 r, 128 r + 128) of the 256-row weight tile in
+// its shared memory, and receives the 128 x 256 fp32 accumulator of its rows
+// in its tensor memory.  Per SM and K tile that is 16 KB of activations and
+// 16 KB of weights for the work that takes 16 + 32 KB with one CTA per tile,
+// which matters because the tensor cores outrun what one SM's TMA can load.
+//
+// Warp roles per CTA (both CTAs run every role but the MMA issuer):
+//   warp 0       TMA producer for this CTA's halves (completing on the even
+//                CTA's barrier, which the MMA issuer waits on) and the scale
+//                atoms (completing on this CTA's own barrier);
+//   warp 1       TMEM allocation (collective over the pair); in the even CTA
+//                one lane issues the pair MMAs and commits them to the
+//                barriers of both CTAs (multicast);
+//   warps 2..5   scale-factor writers: tcgen05.st of this CTA's activation
+//                scale atom and of both weight scale atoms (all 256 columns, in
+//                order: each CTA's half of the pair MMA reads the scales from
+//                its own tensor memory), then an arrive on the even CTA's
+//                sf_ready barrier;
+//   warps 6..13  epilogue: drain this CTA's accumulator as bf16, arrive on the
+//                even CTA's acc_empty barrier, TMA-store the rows.
+// Every wait is bounded; a cluster barrier at the start (barrier
+// initialisation) and at the end (before deallocation) is reached on every path.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mx_kernels.h"
+#include "mx_layout.cuh"
+#include "mx_ptx.cuh"
+
+namespace mx {
+
+namespace {
+
+constexpr int PBM = 128;    // activation rows per CTA (256 per pair)
+constexpr int PBK = 128;    // K elements per stage
+constexpr int PBN = 256;    // output columns per pair tile; each CTA loads PBN / 2 weight rows
+constexpr int PSTAGES = 6;
+constexpr int P_A_BYTES = PBM * PBK;
+constexpr int P_B_BYTES = (PBN / 2) * PBK;
+constexpr int P_SFA_BYTES = kAtomBytes;
+constexpr int P_SFB_BYTES = 2 * kAtomBytes;
+constexpr int P_SF_WARPS = 4;
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_EPI_THREADS = P_EPI_WARPS * 32;
+constexpr int P_EPI_COLS = PBN / (P_EPI_WARPS / 4);
+constexpr int P_STAGE_OUT = 32 * 32 * 2;
+constexpr int P_THREADS = 64 + P_SF_WARPS * 32 + P_EPI_THREADS;
+constexpr int P_OFF_A = 0;
+constexpr int P_OFF_B = P_OFF_A + PSTAGES * P_A_BYTES;
+constexpr int P_OFF_SFA = P_OFF_B + PSTAGES * P_B_BYTES;
+constexpr int P_OFF_SFB = P_OFF_SFA + PSTAGES * P_SFA_BYTES;
+constexpr int P_OFF_OUT = P_OFF_SFB + PSTAGES * P_SFB_BYTES;
+constexpr int P_OFF_BAR = P_OFF_OUT + P_EPI_WARPS * P_STAGE_OUT;
+// per stage: full (operands of both CTAs, in the even CTA), sf_full (this CTA's
+// scale atoms), sf_ready (in the even CTA), empty; then acc_full, acc_empty
+constexpr int P_NUM_BARS = 4 * PSTAGES + 2;
+constexpr int P_OFF_MISC = P_OFF_BAR + P_NUM_BARS * 8;
+constexpr int P_SMEM_USED = P_OFF_MISC + 16;
+constexpr int P_SMEM_ALLOC = P_SMEM_USED + 1024;
+constexpr int P_T_ACC = 0;
+constexpr int P_T_SFA = PBN;
+constexpr int P_T_SFB = P_T_SFA + PSTAGES * 4;
+constexpr int P_T_END = P_T_SFB + PSTAGES * 8;
+constexpr int P_TMEM_COLS = 512;
+static_assert(P_T_END <= P_TMEM_COLS, "tensor memory overflow");
+static_assert(P_SMEM_ALLOC <= 232448, "shared memory overflow");
+
+struct PArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const __nv_bfloat16* bias;
+  int B, M, N, K;
+  int MT2, NT, KT;  // 256-row pair tiles, 256-column tiles, K tiles
+  int RTA, RTB;     // 128-row atom tiles of A and of W
+  int total_tiles;
+};
+
+__device__ __forceinline__ void pair_tile_coords(int tile, const PArgs& a, int& b, int& mt2, int& nt) {
+  const int per_b = a.MT2 * a.NT;
+  b = tile / per_b;
+  const int t = tile - b * per_b;
+  nt = t / a.MT2;
+  mt2 = t - nt * a.MT2;
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
+    gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmOut, const PArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_OFF_BAR);
+  uint64_t* sf_full = full + PSTAGES;
+  uint64_t* sf_ready = sf_full + PSTAGES;
+  uint64_t* empty = sf_ready + PSTAGES;
+  uint64_t* acc_full = empty + PSTAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P_OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P_OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;  // clusters are (2, 1, 1)
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&full[s], 2);                        // both producers (even CTA's copy is used)
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_ready[s], 2 * P_SF_WARPS);       // one arrive per writer warp of both CTAs
+      mbar_init(&empty[s], 1);                       // the even CTA's commit
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * P_EPI_WARPS);           // one arrive per epilogue warp of both CTAs
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anyone arrives remotely
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
+        int b, mt2, nt;
+        pair_tile_coords(tile, args, b, mt2, nt);
+        const int rt_a = mt2 * 2 + static_cast<int>(rank);  // this CTA's activation atom row tile
+        const bool has_sfa = rt_a < args.RTA;
+        const int nb_atoms = min(2, args.RTB - nt * 2);
+        const uint32_t sf_tx = (has_sfa ? P_SFA_BYTES : 0) + nb_atoms * kAtomBytes;
+        for (int kt = 0; kt < args.KT; ++kt) {
+          if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          // scale atoms: this CTA's own barrier, so that the writers move them
+          // to TMEM while the operands are still loading
+          const int64_t arow = static_cast<int64_t>(b) * args.KT + kt;
+          mbar_arrive_expect_tx(&sf_full[stage], sf_tx);
+          if (has_sfa)
+            bulk_load(smem + P_OFF_SFA + stage * P_SFA_BYTES, args.sfa + (arow * args.RTA + rt_a) * kAtomBytes,
+                      P_SFA_BYTES, &sf_full[stage]);
+          bulk_load(smem + P_OFF_SFB + stage * P_SFB_BYTES,
+                    args.sfb + (arow * args.RTB + static_cast<int64_t>(nt) * 2) * kAtomBytes,
+                    nb_atoms * kAtomBytes, &sf_full[stage]);
+          // operands: both CTAs' loads complete on the even CTA's barrier, which
+          // the MMA issuer waits on directly
+          const uint32_t full_even = map_shared_rank(smem_u32(&full[stage]), 0);
+          mbar_arrive_expect_tx_cluster(full_even, P_A_BYTES + P_B_BYTES);
+          tma_load_3d_cluster_bar(smem + P_OFF_A + stage * P_A_BYTES, &tmA, full_even, kt * PBK, rt_a * PBM, b);
+          tma_load_3d_cluster_bar(smem + P_OFF_B + stage * P_B_BYTES, &tmB, full_even, kt * PBK,
+                                  nt * PBN + static_cast<int>(rank) * (PBN / 2), b);
+          ++issued;
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Copies this thread started must land, and every commit the even CTA
+      // sent to this CTA's empty barriers must have arrived, before exit (the
+      // last commit of a stage follows the MMA that consumed its operands).
+      for (int s = 0; s < PSTAGES; ++s) {
+        if (issued <= s) continue;
+        const int64_t last = ((issued - 1 - s) / PSTAGES) * PSTAGES + s;
+        const uint32_t par = static_cast<uint32_t>((last / PSTAGES) & 1);
+        mbar_wait(&sf_full[s], par, nullptr);
+        mbar_wait_cluster(&empty[s], par, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      const uint32_t idesc0 = idesc_mxf8(2 * PBM, PBN);
+      for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
+        if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < args.KT; ++kt) {
+          // operands of both CTAs landed, and both CTAs' scales are in TMEM
+          if (!mbar_wait_cluster(&full[stage], phase, abort_flag) ||
+              !mbar_wait_cluster(&sf_ready[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(smem + P_OFF_A + stage * P_A_BYTES));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + P_OFF_B + stage * P_B_BYTES));
+          const uint32_t t_sfa = tmem + P_T_SFA + stage * 4;
+          const uint32_t t_sfb = tmem + P_T_SFB + stage * 8;
+#pragma unroll
+          for (int kk = 0; kk < PBK / 32; ++kk)
+            tc_mma_mxf8_pair(tmem + P_T_ACC, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk),
+                             t_sfa, t_sfb, (kt | kk) != 0);
+          tc_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == PSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(acc_full, 0x3);
+        acc_phase ^= 1u;
+      }
+      if (!ok) __nanosleep(200000);  // let issued tensor-core work retire
+    }
+    __syncwarp();
+  } else if (warp < 2 + P_SF_WARPS) {
+    // ------------------------------------------------------------ scale-factor writers
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t ready_base = map_shared_rank(smem_u32(sf_ready), 0);  // the even CTA's barriers
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = pair; tile < args.total_tiles; tile += npairs) {
+      int b, mt2, nt;
+      pair_tile_coords(tile, args, b, mt2, nt);
+      const bool has_sfa = mt2 * 2 + static_cast<int>(rank) < args.RTA;
+      const int nb_atoms = min(2, args.RTB - nt * 2);
+      bool ok = true;
+      for (int kt = 0; kt < args.KT; ++kt) {
+        if (!mbar_wait(&sf_full[stage], phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa = smem + P_OFF_SFA + stage * P_SFA_BYTES + lane * 16;
+        const uint8_t* sfb = smem + P_OFF_SFB + stage * P_SFB_BYTES + lane * 16;
+        const uint4 va = has_sfa ? *reinterpret_cast<const uint4*>(sfa) : make_uint4(0, 0, 0, 0);
+        tmem_st_32x32b_x4(lane_base + P_T_SFA + stage * 4, va.x, va.y, va.z, va.w);
+        // weight scales for all 256 columns, in column order: each CTA's half
+        // of the pair MMA reads them from its own tensor memory
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint4 vb = j < nb_atoms ? *reinterpret_cast<const uint4*>(sfb + j * kAtomBytes)
+                                        : make_uint4(0, 0, 0, 0);
+          tmem_st_32x32b_x4(lane_base + P_T_SFB + stage * 8 + 4 * j, vb.x, vb.y, vb.z, vb.w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(ready_base + static_cast<uint32_t>(stage * 8));
+        if (++stage == PSTAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2 - P_SF_WARPS;
+    const int quad = warp & 3;
+    const int col0 = (ew >> 2) * P_EPI_COLS;
+    uint8_t* stage_out = smem + P_OFF_OUT + ew * P_STAGE_OUT;
+    const uint32_t acc_empty_even = map_shared_rank(smem_u32(acc_empty), 0);
+    uint32_t acc_phase = 0;
+    bool pending = false;
+    for (int tile = pair; tile < args.total_tiles; tile += npairs) {
+      int b, mt2, nt;
+      pair_tile_coords(tile, args, b, mt2, nt);
+      if (!mbar_wait_cluster(acc_full, acc_phase, abort_flag)) break;
+      tc_fence_after();
+      uint32_t packed[P_EPI_COLS / 2];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + P_T_ACC + col0;
+#pragma unroll
+      for (int c = 0; c < P_EPI_COLS / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int n0 = nt * PBN + col0 + c * 32;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float bv[8];
+          const int n = n0 + 8 * g;
+          if (args.bias != nullptr && n < args.N) {
+            const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
+            const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              bv[2 * i] = __uint_as_float(bw[i] << 16);
+              bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bv[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            packed[c * 16 + g * 4 + i] = pack_bf16x2(__uint_as_float(r[8 * g + 2 * i]) + bv[2 * i],
+                                                     __uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even);  // the even CTA may start the next tile
+      acc_phase ^= 1u;
+
+      const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;
+#pragma unroll
+      for (int c = 0; c < P_EPI_COLS / 32; ++c) {
+        if (lane == 0 && pending) bulk_wait_group_read0();
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(packed[c * 16 + 4 * q], packed[c * 16 + 4 * q + 1], packed[c * 16 + 4 * q + 2],
+                              packed[c * 16 + 4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmOut, stage_out, nt * PBN + col0 + c * 32, row0, b);
+          bulk_commit_group();
+          pending = true;
+        }
+      }
+    }
+    if (lane == 0 && pending) bulk_wait_group0();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA of the pair leaves while the other may still signal it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, P_TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_mxf8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         P_SMEM_ALLOC);
+    if (e != cudaSuccess) {
+      *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      return e;
+    }
+    attr_set[dev] = true;
+  }
+  CUtensorMap ma, mb, mo;
+  cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, PBM, msg);
+  if (e != cudaSuccess) return e;
+  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg);
+  if (e != cudaSuccess) return e;
+  e = make_output_map(&mo, p.out, p.B, p.M, p.N, msg);
+  if (e != cudaSuccess) return e;
+
+  PArgs a;
+  a.sfa = p.sfa;
+  a.sfb = p.sfb;
+  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.B = static_cast<int>(p.B);
+  a.M = static_cast<int>(p.M);
+  a.N = static_cast<int>(p.N);
+  a.K = static_cast<int>(p.K);
+  a.MT2 = static_cast<int>(ceil_div(p.M, 2 * PBM));
+  a.NT = static_cast<int>(ceil_div(p.N, PBN));
+  a.KT = static_cast<int>(p.K / PBK);
+  a.RTA = static_cast<int>(ceil_div(p.M, kAtomRows));
+  a.RTB = static_cast<int>(ceil_div(p.N, kAtomRows));
+  a.total_tiles = a.B * a.MT2 * a.NT;
+  const int pairs = a.total_tiles < sms / 2 ? a.total_tiles : sms / 2;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, a);
+  if (e != cudaSuccess) *msg = "pair GEMM launch failed";
+  return e;
+}
+
+}  // namespace mx
+
+namespace mx {
+
+cudaError_t take_status_pair(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mx

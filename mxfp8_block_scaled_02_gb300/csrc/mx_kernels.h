@@ -28,10 +28,16 @@ struct GemmProblem {
   const void* bias;  // bf16 [N] or nullptr
   void* out;         // bf16 [B, M, N]
   int64_t B, M, N, K;
+  int tiles = 0;     // 0 or 1: one CTA per 128 x 256 tile; 2: 256 x 256 tiles on CTA pairs
 };
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
 cudaError_t take_status_gemm(unsigned int* out);
+// gemm_pair.cu: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2).
+cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
+cudaError_t take_status_pair(unsigned int* out);
+// bf16 [B][M][N] output map, box {32 columns, 32 rows, 1} (gemm.cu).
+cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, int64_t N, const char** msg);
 // 3-D TMA map over [B][rows][K] E4M3 bytes, box {128, box_rows, 1}, 128-byte swizzle.
 cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
                              int64_t K, int box_rows, const char** msg);

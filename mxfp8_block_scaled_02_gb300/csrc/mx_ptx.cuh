@@ -60,6 +60,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending test with cluster-scope acquire, for barriers that other CTAs
+// of the cluster arrive on: a thread suspended in try_wait is not woken
+// promptly by an arrival from another CTA, so these waits poll instead.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Arrive with an expected transaction count on a barrier of another CTA of
+// the cluster (`addr` from map_shared_rank).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(addr),
+               "r"(bytes)
+               : "memory");
+}
+
+// TMA load into this CTA's shared memory that completes on a barrier of either
+// CTA of the pair (cta_group::2 form; `bar_addr` from map_shared_rank).
+__device__ __forceinline__ void tma_load_3d_cluster_bar(void* dst, const CUtensorMap* m, uint32_t bar_addr,
+                                                        int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(bar_addr), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Arrive (release, cluster scope) on the barrier at `addr` in CTA space of
+// the cluster (from map_shared_rank).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
 // Wait for the phase with parity `parity` to complete, for at most
 // kWaitLimitNs, or until *abort becomes non-zero.  On failure sets the device
 // status word and *abort, and returns false.
@@ -81,6 +121,28 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort);
+}
+
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity,
+                                                           volatile int* abort) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_status, kStatusTimeout);
+      if (abort != nullptr) *abort = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded wait with cluster-scope acquire (see mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cluster_slow(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------- TMA / bulk
@@ -157,6 +219,48 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Pair (cta_group::2) forms: allocation and deallocation are collective, one
+// warp in each CTA of the pair; the MMA is issued by one thread of the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Arrive once on `bar` (same offset) in every CTA of `cta_mask` when all prior
+// pair MMAs of this thread finish.
+__device__ __forceinline__ void tc_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// D (TMEM of both CTAs) (+)= A x B^T over the CTA pair: M = 256 (128 rows
+// from each CTA's shared memory), N split in halves between the two CTAs.
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t sfa_taddr, uint32_t sfb_taddr,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_taddr),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_taddr), "r"(sfb_taddr)
+      : "memory");
 }
 
 // Arrive once on `bar` when all prior tcgen05 async ops of this thread finish.

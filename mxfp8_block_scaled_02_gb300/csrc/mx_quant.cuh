@@ -29,9 +29,10 @@ namespace mx {
 // Returns the block's scale byte (same in the four lanes) and the 8 codes.
 __device__ __forceinline__ uint32_t quantize_quarter_block(const uint4 v, uint2& codes) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t amax = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  // |x| of both halves at once; unsigned 16-bit max per half
+  uint32_t m2 = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+  uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
   amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
 

@@ -16,43 +16,52 @@ namespace mx {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;  // independent 8-block tasks in flight per warp
+constexpr int kQuantUnroll = 4;  // 8-block tasks per work item, loads all in flight
 
-// One warp task = 8 consecutive 32-element blocks of one row (256 values,
-// 512 bytes of bf16).  Lane l owns 8 values: block j = l / 4 of the task,
-// quarter l % 4 of that block; four lanes combine their amax by shuffles.
+// A task is 8 consecutive 32-element blocks of one row (256 values, 512
+// bytes of bf16); lane l owns 8 values: block j = l / 4 of the task, quarter
+// l % 4 of that block, and four lanes combine their amax by shuffles.  A work
+// item is kQuantUnroll consecutive tasks of one row, so the row (and, for the
+// packed layout, its batch and atom row) is found with one division per item.
 // kPacked selects the scale output: false = row-major [rows, K/32], true = the
 // 512-byte atom layout of mx_layout.cuh (rows grouped per batch of rows_per_b).
-// All index arithmetic is warp-uniform 32-bit except the final byte offsets.
 template <bool kPacked>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
-    const uint4* __restrict__ x, uint32_t KB, uint32_t tasks_per_row, uint32_t ntasks,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT,
-    uint32_t KT) {
+    const uint4* __restrict__ x, uint32_t KB, uint32_t tasks_per_row, uint32_t items_per_row,
+    uint32_t nitems, uint8_t* __restrict__ q, uint8_t* __restrict__ s, uint32_t rows_per_b,
+    uint32_t RT, uint32_t KT) {
   const int lane = threadIdx.x & 31;
-  const int j = lane >> 2, part = lane & 3;
+  const uint32_t j = lane >> 2, part = lane & 3;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t atom_k_stride = static_cast<int64_t>(RT) * kAtomBytes;  // next K tile, same rows
 
-  for (uint32_t t0 = warp * kQuantUnroll; t0 < ntasks; t0 += nwarps * kQuantUnroll) {
+  for (uint32_t item = warp; item < nitems; item += nwarps) {
+    const uint32_t row = item / items_per_row;
+    const uint32_t t0 = (item - row * items_per_row) * kQuantUnroll;
+    const int64_t row_blk = static_cast<int64_t>(row) * KB;  // first block of the row
     uint4 v[kQuantUnroll];
-    uint32_t row[kQuantUnroll], kb[kQuantUnroll];
-    bool valid[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t t = t0 + u;
-      row[u] = t / tasks_per_row;
-      kb[u] = (t - row[u] * tasks_per_row) * 8 + j;
-      valid[u] = t < ntasks && kb[u] < KB;
-      const int64_t blk = static_cast<int64_t>(row[u]) * KB + kb[u];
-      v[u] = valid[u] ? __ldg(x + blk * 4 + part) : make_uint4(0, 0, 0, 0);
+      const uint32_t kb = (t0 + u) * 8 + j;
+      const bool valid = t0 + u < tasks_per_row && kb < KB;
+      v[u] = valid ? __ldg(x + (row_blk + kb) * 4 + part) : make_uint4(0, 0, 0, 0);
+    }
+    int64_t atom_row = 0;  // packed: offset of (row, block 0) in its first atom
+    if (kPacked) {
+      const uint32_t b = row / rows_per_b, r = row - b * rows_per_b;
+      atom_row = (static_cast<int64_t>(b) * KT * RT + (r >> 7)) * kAtomBytes + (r & 31) * 16 +
+                 ((r >> 5) & 3) * 4;
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      uint2 out;
-      const uint32_t sbyte = quantize_quarter_block(v[u], out);
-      const int64_t blk = static_cast<int64_t>(row[u]) * KB + kb[u];
-      if (valid[u]) *reinterpret_cast<uint2*>(q + blk * 32 + part * 8) = out;
+      const uint32_t task = t0 + u;
+      const uint32_t kb_task = task * 8;
+      const uint32_t kb = kb_task + j;
+      const bool valid = task < tasks_per_row && kb < KB;
+      uint2 codes;
+      const uint32_t sbyte = quantize_quarter_block(v[u], codes);
+      if (valid) *reinterpret_cast<uint2*>(q + (row_blk + kb) * 32 + part * 8) = codes;
 
       // Scale bytes: gather the task's 8 bytes (lanes 0, 4, ..., 28) so that
       // whole words are stored when the task is complete.
@@ -61,24 +70,22 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
       const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 8);
       const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 12);
       const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-      const uint32_t kb_task = kb[u] - j;  // first block of the task
-      const bool full_task = kb_task + 8 <= KB;
+      const bool full_task = task < tasks_per_row && kb_task + 8 <= KB;
       if (kPacked) {
-        // blocks kb_task..+3 and kb_task+4..+7 are 4 consecutive bytes of two atoms
-        const uint32_t b = row[u] / rows_per_b, r = row[u] - b * rows_per_b;
+        // blocks kb..kb+3 (kb % 4 == 0) are 4 consecutive bytes of one atom
         if (full_task) {
-          if (valid[u] && (lane & 15) == 0)
-            *reinterpret_cast<uint32_t*>(s + sf_packed_offset(b, r, kb[u], RT, KT)) = word;
-        } else if (valid[u] && part == 0) {
-          s[sf_packed_offset(b, r, kb[u], RT, KT)] = static_cast<uint8_t>(sbyte);
+          if ((lane & 15) == 0)
+            *reinterpret_cast<uint32_t*>(s + atom_row + (kb >> 2) * atom_k_stride) = word;
+        } else if (valid && part == 0) {
+          s[atom_row + (kb >> 2) * atom_k_stride + (kb & 3)] = static_cast<uint8_t>(sbyte);
         }
       } else {
         const uint32_t hi_word = __shfl_sync(0xFFFFFFFFu, word, 16);
-        const int64_t off = static_cast<int64_t>(row[u]) * KB + kb_task;
+        const int64_t off = row_blk + kb_task;
         if (full_task && (off & 7) == 0) {
-          if (valid[u] && lane == 0) *reinterpret_cast<uint2*>(s + off) = make_uint2(word, hi_word);
-        } else if (valid[u] && part == 0) {
-          s[static_cast<int64_t>(row[u]) * KB + kb[u]] = static_cast<uint8_t>(sbyte);
+          if (lane == 0) *reinterpret_cast<uint2*>(s + off) = make_uint2(word, hi_word);
+        } else if (valid && part == 0) {
+          s[row_blk + kb] = static_cast<uint8_t>(sbyte);
         }
       }
     }
@@ -143,9 +150,10 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
   (void)B;
   const int64_t KB = K / 32;
   const int64_t tasks_per_row = ceil_div(KB, 8);
-  const int64_t ntasks = rows * tasks_per_row;
-  if (ntasks == 0) return cudaSuccess;
-  if (ntasks > 0x7FFFFFFFll || KB > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  const int64_t items_per_row = ceil_div(tasks_per_row, kQuantUnroll);
+  const int64_t nitems = rows * items_per_row;
+  if (nitems == 0) return cudaSuccess;
+  if (nitems > 0x7FFFFFFFll || KB > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   static int per_sm[2] = {0, 0};
   int& occ = per_sm[packed_scales ? 1 : 0];
   if (occ == 0) {
@@ -154,18 +162,19 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<false>, kQuantThreads, 0);
     if (e != cudaSuccess || occ < 1) occ = 1;
   }
-  const int64_t warps_needed = ceil_div(ntasks, kQuantUnroll);
-  const int grid = grid_for(warps_needed * 32, kQuantThreads, sms, occ);
+  const int grid = grid_for(nitems * 32, kQuantThreads, sms, occ);
   const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
   const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
   if (packed_scales)
     quantize_kernel<true><<<grid, kQuantThreads, 0, stream>>>(
         static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
-        static_cast<uint32_t>(ntasks), q, s, static_cast<uint32_t>(rows_per_b), RT, KT);
+        static_cast<uint32_t>(items_per_row), static_cast<uint32_t>(nitems), q, s,
+        static_cast<uint32_t>(rows_per_b), RT, KT);
   else
     quantize_kernel<false><<<grid, kQuantThreads, 0, stream>>>(
         static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
-        static_cast<uint32_t>(ntasks), q, s, static_cast<uint32_t>(rows_per_b), RT, KT);
+        static_cast<uint32_t>(items_per_row), static_cast<uint32_t>(nitems), q, s,
+        static_cast<uint32_t>(rows_per_b), RT, KT);
   return cudaGetLastError();
 }
 

@@ -171,7 +171,8 @@ def linear(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
     given, the pre-quantised E4M3 ``x_q [..., K]`` with row-major scales
     ``[..., K/32]``.  For batched weights (``[B, N, K]``) x is ``[B, M, K]``.
     Returns bf16 ``[..., N]``.  ``path`` forces the small-M (1) or large-M (2)
-    kernel path; 0 lets the library choose.
+    kernel path, or the large-M path on CTA-pair tiles (3); 0 lets the library
+    choose.
     """
     quantized = x_scale is not None
     if not quantized and x.dtype != torch.bfloat16:

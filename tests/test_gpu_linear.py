@@ -303,3 +303,30 @@ def test_small_m_path_refuses_what_it_cannot_do():
     with pytest.raises(ops.MxStatusError):            # M > 64
         ops.linear(bf16_to_dev(big.x[0], dev), pw, path=1)
     ops.check()
+
+
+# ------------------------------------------------------------------ CTA-pair tiles at large M
+@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (300, 520, 512)])
+def test_single_cta_tiles_exact_scales(M, N, K):
+    """The large-M path on the exact scale-pattern problem with one CTA per
+    128 x 256 tile (path 2) and with 256 x 256 tiles on CTA pairs (path 3)."""
+    KB = K // 32
+    m = np.arange(M)[:, None]
+    n = np.arange(N)[:, None]
+    kb = np.arange(KB)[None, :]
+    sx = (127 + (m * 3 + kb * 5) % 7 - 3).astype(np.uint8)
+    sw = (127 + (n * 5 + kb * 2) % 9 - 4).astype(np.uint8)
+    one = oracle.e4m3_encode(np.ones(1))[0]
+    xq = np.full((M, K), one, np.uint8)
+    wq = np.full((N, K), one, np.uint8)
+    xq[:, 1::3] |= 0x80
+    exp = _exact_bits(oracle.linear(xq, sx, wq, sw))
+    for path in (2, 3):
+        got = bf16_bits(_run_prequant(xq, sx, wq, sw, path=path))
+        assert np.array_equal(got, exp), f"path {path}: {int((got != exp).sum())} mismatches"
+
+
+def test_pair_tiles_ragged_batched_bias():
+    p = synth.make_problem("pair-rag", 3, 300, 520, 640, seed=19, bias_std=0.1)
+    _bf16_problem_check(p, path=2)
+    _bf16_problem_check(p, path=3)
