@@ -144,6 +144,25 @@ def _traffic_for_current_gemm():
         return None
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time.
+
+    Every rank runs the same step on its own GPU (independent replicas: the
+    layer has no exchange step), so the job does world * steps steps.
+    """
+    return flops_per_step * world * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def _dev_bf16(bits: np.ndarray, dev) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -257,13 +276,9 @@ def run_ours(args):
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(n)]
     q_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
     g_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / n
-    value = flops * world * n / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops, n, world, total_ms)
 
     gemm_ms = statistics.mean(g_ms)
     quant_ms = statistics.mean(q_ms)
