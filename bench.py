@@ -49,8 +49,8 @@ WORKLOAD = "prefill MLP-up M4096 N14336 K4096, bf16 x quantised in the step, no 
 FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_prefill_up.traffic.txt")
-GEMM_SOURCE = os.path.join(ROOT, "mxfp8_block_scaled_02_gb300", "csrc", "gemm.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_pair_prefill_up.traffic.txt")
+GEMM_SOURCE = os.path.join(ROOT, "mxfp8_block_scaled_02_gb300", "csrc", "gemm_pair.cu")
 
 
 def _dist_env():
@@ -133,11 +133,11 @@ class ClockSampler:
 
 
 def _traffic_for_current_gemm():
-    """Per-launch DRAM bytes from the committed ncu summary, if it matches gemm.cu."""
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches gemm_pair.cu."""
     try:
         kv = dict(line.split("=", 1) for line in open(TRAFFIC_FILE).read().split() if "=" in line)
         src_hash = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()[:16]
-        if kv.get("gemm_cu_sha256_16") != src_hash:
+        if kv.get("source_sha256_16") != src_hash:
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -343,7 +343,7 @@ def run_ours(args):
             "fp8_peak_fraction": value / fp8_peak,
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                          "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": traffic,
-                         "kernel": "gemm_mxf8_kernel (tcgen05 kind::mxf8f6f4 block_scale)",
+                         "kernel": "gemm_mxf8_pair_kernel (tcgen05.mma.cta_group::2 kind::mxf8f6f4 block_scale)",
                          "peak_source": f"{peak_src} bf16 burst x {FP8_PER_BF16:g} (nominal FP8/BF16)"},
             "kernels": {"quantize_us": quant_ms * 1e3,
                         "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9,

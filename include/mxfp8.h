@@ -151,9 +151,10 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * mxfp8_linear_path - mxfp8_linear with the kernel path chosen by the caller
  * instead of by M: path 0 = automatic (as mxfp8_linear), 1 = small-M path
  * (quantisation fused into the GEMM, weights on the MMA's M side), 2 = large-M
- * path (separate quantise kernel, then the GEMM with one CTA per 128 x 256
- * tile), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
- * cta_group::2; not yet faster, kept selectable and tested).  All paths
+ * path with one CTA per 128 x 256 output tile (separate quantise kernel, then
+ * the GEMM), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
+ * cta_group::2; what path 0 takes for M > 128 when the small-M path does not
+ * apply).  All paths
  * compute the same function; this exists so that tests can check each on
  * every shape.  Path 1 needs M <= 64 and x_bf16 (else MXFP8_ERR_UNSUPPORTED).
  */

@@ -265,7 +265,7 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
     e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
-  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : 1};
+  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0)};
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);
   if (e != cudaSuccess) return cuda_fail(e, msg);

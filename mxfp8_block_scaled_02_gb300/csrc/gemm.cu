@@ -395,7 +395,9 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, i
 }
 
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
-  if (p.tiles == 2) return launch_gemm_pair(p, sms, stream, msg);
+  // 256 x 256 tiles on CTA pairs load 32 KB per SM and K tile against 48 KB
+  // for 128 x 256 tiles on one CTA, and measure faster once M spans a pair tile.
+  if (p.tiles == 2 || (p.tiles == 0 && p.M > 128 && sms >= 2)) return launch_gemm_pair(p, sms, stream, msg);
   using C = PrefillCfg;
   static bool attr_set[64] = {};
   int dev = 0;

@@ -13,21 +13,26 @@
 // which matters because the tensor cores outrun what one SM's TMA can load.
 //
 // Warp roles per CTA (both CTAs run every role but the MMA issuer):
-//   warp 0       TMA producer for this CTA's halves (completing on the even
-//                CTA's barrier, which the MMA issuer waits on) and the scale
-//                atoms (completing on this CTA's own barrier);
+//   warp 0       TMA producer for this CTA's operand halves; both CTAs' copies
+//                complete on the even CTA's `full` barrier, whose transaction
+//                count the even CTA alone posts (for both), so the odd CTA
+//                sends no barrier traffic of its own;
 //   warp 1       TMEM allocation (collective over the pair); in the even CTA
 //                one lane issues the pair MMAs and commits them to the
 //                barriers of both CTAs (multicast);
-//   warps 2..5   scale-factor writers: tcgen05.st of this CTA's activation
-//                scale atom and of both weight scale atoms (all 256 columns, in
-//                order: each CTA's half of the pair MMA reads the scales from
-//                its own tensor memory), then an arrive on the even CTA's
-//                sf_ready barrier;
+//   warps 2..5   scale-factor writers: read this CTA's activation scale atom
+//                and both weight scale atoms straight from global memory a few
+//                K tiles ahead, and once a pair of stages is free tcgen05.st
+//                them (all 256 weight columns, in order: each CTA's half of
+//                the pair MMA reads the scales from its own tensor memory),
+//                then arrive on the even CTA's sf_ready barrier of the pair;
 //   warps 6..13  epilogue: drain this CTA's accumulator as bf16, arrive on the
 //                even CTA's acc_empty barrier, TMA-store the rows.
-// Every wait is bounded; a cluster barrier at the start (barrier
-// initialisation) and at the end (before deallocation) is reached on every path.
+// One thread issuing every copy of a stage is the first limit here (a TMA or
+// bulk-copy issue costs ~100-150 cycles, a stage of MMAs ~550), which is why
+// the scale atoms do not go through the producer.  Every wait is bounded; a
+// cluster barrier at the start (barrier initialisation) and at the end (before
+// deallocation) is reached on every path.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -46,9 +51,8 @@ constexpr int PBN = 256;    // output columns per pair tile; each CTA loads PBN 
 constexpr int PSTAGES = 6;
 constexpr int P_A_BYTES = PBM * PBK;
 constexpr int P_B_BYTES = (PBN / 2) * PBK;
-constexpr int P_SFA_BYTES = kAtomBytes;
-constexpr int P_SFB_BYTES = 2 * kAtomBytes;
 constexpr int P_SF_WARPS = 4;
+constexpr int P_SF_AHEAD = 2;  // stage pairs of scale atoms each writer holds in registers
 constexpr int P_EPI_WARPS = 8;
 constexpr int P_EPI_THREADS = P_EPI_WARPS * 32;
 constexpr int P_EPI_COLS = PBN / (P_EPI_WARPS / 4);
@@ -56,13 +60,11 @@ constexpr int P_STAGE_OUT = 32 * 32 * 2;
 constexpr int P_THREADS = 64 + P_SF_WARPS * 32 + P_EPI_THREADS;
 constexpr int P_OFF_A = 0;
 constexpr int P_OFF_B = P_OFF_A + PSTAGES * P_A_BYTES;
-constexpr int P_OFF_SFA = P_OFF_B + PSTAGES * P_B_BYTES;
-constexpr int P_OFF_SFB = P_OFF_SFA + PSTAGES * P_SFA_BYTES;
-constexpr int P_OFF_OUT = P_OFF_SFB + PSTAGES * P_SFB_BYTES;
+constexpr int P_OFF_OUT = P_OFF_B + PSTAGES * P_B_BYTES;
 constexpr int P_OFF_BAR = P_OFF_OUT + P_EPI_WARPS * P_STAGE_OUT;
-// per stage: full (operands of both CTAs, in the even CTA), sf_full (this CTA's
-// scale atoms), sf_ready (in the even CTA), empty; then acc_full, acc_empty
-constexpr int P_NUM_BARS = 4 * PSTAGES + 2;
+// per stage: full (operands of both CTAs, in the even CTA) and empty; per
+// stage pair: sf_ready (in the even CTA); then acc_full, acc_empty
+constexpr int P_NUM_BARS = 2 * PSTAGES + PSTAGES / 2 + 2;
 constexpr int P_OFF_MISC = P_OFF_BAR + P_NUM_BARS * 8;
 constexpr int P_SMEM_USED = P_OFF_MISC + 16;
 constexpr int P_SMEM_ALLOC = P_SMEM_USED + 1024;
@@ -73,6 +75,7 @@ constexpr int P_T_END = P_T_SFB + PSTAGES * 8;
 constexpr int P_TMEM_COLS = 512;
 static_assert(P_T_END <= P_TMEM_COLS, "tensor memory overflow");
 static_assert(P_SMEM_ALLOC <= 232448, "shared memory overflow");
+static_assert(PSTAGES % 2 == 0, "scale factors are written per pair of stages");
 
 struct PArgs {
   const uint8_t* sfa;
@@ -98,10 +101,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_OFF_BAR);
-  uint64_t* sf_full = full + PSTAGES;
-  uint64_t* sf_ready = sf_full + PSTAGES;
-  uint64_t* empty = sf_ready + PSTAGES;
-  uint64_t* acc_full = empty + PSTAGES;
+  uint64_t* empty = full + PSTAGES;
+  uint64_t* sf_ready = empty + PSTAGES;  // one per stage pair
+  uint64_t* acc_full = sf_ready + PSTAGES / 2;
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P_OFF_MISC + 4);
@@ -115,11 +117,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
-      mbar_init(&full[s], 2);                        // both producers (even CTA's copy is used)
-      mbar_init(&sf_full[s], 1);
-      mbar_init(&sf_ready[s], 2 * P_SF_WARPS);       // one arrive per writer warp of both CTAs
+      mbar_init(&full[s], 1);                        // the even CTA's producer (even CTA's copy is used)
       mbar_init(&empty[s], 1);                       // the even CTA's commit
     }
+    for (int s = 0; s < PSTAGES / 2; ++s)
+      mbar_init(&sf_ready[s], 2 * P_SF_WARPS);       // one arrive per writer warp of both CTAs
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * P_EPI_WARPS);           // one arrive per epilogue warp of both CTAs
     *abort_flag = 0;
@@ -148,29 +150,19 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
         int b, mt2, nt;
         pair_tile_coords(tile, args, b, mt2, nt);
-        const int rt_a = mt2 * 2 + static_cast<int>(rank);  // this CTA's activation atom row tile
-        const bool has_sfa = rt_a < args.RTA;
-        const int nb_atoms = min(2, args.RTB - nt * 2);
-        const uint32_t sf_tx = (has_sfa ? P_SFA_BYTES : 0) + nb_atoms * kAtomBytes;
+        const int rt_a = mt2 * 2 + static_cast<int>(rank);  // this CTA's activation row tile
         for (int kt = 0; kt < args.KT; ++kt) {
-          if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort_flag)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          // scale atoms: this CTA's own barrier, so that the writers move them
-          // to TMEM while the operands are still loading
-          const int64_t arow = static_cast<int64_t>(b) * args.KT + kt;
-          mbar_arrive_expect_tx(&sf_full[stage], sf_tx);
-          if (has_sfa)
-            bulk_load(smem + P_OFF_SFA + stage * P_SFA_BYTES, args.sfa + (arow * args.RTA + rt_a) * kAtomBytes,
-                      P_SFA_BYTES, &sf_full[stage]);
-          bulk_load(smem + P_OFF_SFB + stage * P_SFB_BYTES,
-                    args.sfb + (arow * args.RTB + static_cast<int64_t>(nt) * 2) * kAtomBytes,
-                    nb_atoms * kAtomBytes, &sf_full[stage]);
-          // operands: both CTAs' loads complete on the even CTA's barrier, which
-          // the MMA issuer waits on directly
+          // Both CTAs' copies complete on the even CTA's barrier.  The odd
+          // CTA's bytes may land before the even CTA posts the count (the
+          // transaction count goes negative for a while); they cannot land a
+          // phase early, because this stage was freed by a commit that
+          // followed the MMA that waited for the barrier's previous phase.
           const uint32_t full_even = map_shared_rank(smem_u32(&full[stage]), 0);
-          mbar_arrive_expect_tx_cluster(full_even, P_A_BYTES + P_B_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
           tma_load_3d_cluster_bar(smem + P_OFF_A + stage * P_A_BYTES, &tmA, full_even, kt * PBK, rt_a * PBM, b);
           tma_load_3d_cluster_bar(smem + P_OFF_B + stage * P_B_BYTES, &tmB, full_even, kt * PBK,
                                   nt * PBN + static_cast<int>(rank) * (PBN / 2), b);
@@ -181,15 +173,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
         }
       }
-      // Copies this thread started must land, and every commit the even CTA
-      // sent to this CTA's empty barriers must have arrived, before exit (the
-      // last commit of a stage follows the MMA that consumed its operands).
+      // Every commit the even CTA sends to this CTA's empty barriers must have
+      // arrived before exit; the last commit of a stage follows the MMA that
+      // waited for its operands, so the copies have landed too.
       for (int s = 0; s < PSTAGES; ++s) {
         if (issued <= s) continue;
         const int64_t last = ((issued - 1 - s) / PSTAGES) * PSTAGES + s;
         const uint32_t par = static_cast<uint32_t>((last / PSTAGES) & 1);
-        mbar_wait(&sf_full[s], par, nullptr);
-        mbar_wait_cluster(&empty[s], par, nullptr);
+        mbar_wait(&empty[s], par, nullptr);
       }
     }
     __syncwarp();
@@ -201,15 +192,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       bool ok = true;
       const uint32_t idesc0 = idesc_mxf8(2 * PBM, PBN);
       for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
-        if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int kt = 0; kt < args.KT; ++kt) {
           // operands of both CTAs landed, and both CTAs' scales are in TMEM
-          if (!mbar_wait_cluster(&full[stage], phase, abort_flag) ||
-              !mbar_wait_cluster(&sf_ready[stage], phase, abort_flag)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag) ||
+              !mbar_wait(&sf_ready[stage >> 1], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -237,43 +228,97 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     __syncwarp();
   } else if (warp < 2 + P_SF_WARPS) {
     // ------------------------------------------------------------ scale-factor writers
+    // Each writer warp owns TMEM lanes [32 (warp % 4), +32) and writes the
+    // same atom lines there (one 16-byte line per lane and atom).  Each K
+    // tile's atoms are fetched P_SF_AHEAD K tiles before they are written; the
+    // write waits for the stage's previous MMAs (empty barrier).
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t ready_base = map_shared_rank(smem_u32(sf_ready), 0);  // the even CTA's barriers
+    const uint32_t ready_even = map_shared_rank(smem_u32(sf_ready), 0);
+    const int my_tiles = pair < args.total_tiles ? (args.total_tiles - 1 - pair) / npairs + 1 : 0;
+    const int64_t total = static_cast<int64_t>(my_tiles) * args.KT;
+    // Fetch cursor: pointers to this lane's line of the activation atom and
+    // of the first weight atom of K tile f_kt of tile f_tile; advancing a K
+    // tile adds one K-tile row of atoms.
+    int f_tile = pair, f_kt = 0;
+    const uint8_t* f_a = nullptr;
+    const uint8_t* f_w = nullptr;
+    bool f_has_a = false, f_has_w1 = false;
+    const int64_t a_step = static_cast<int64_t>(args.RTA) * kAtomBytes;
+    const int64_t w_step = static_cast<int64_t>(args.RTB) * kAtomBytes;
+    auto start_tile = [&]() {
+      if (f_tile >= args.total_tiles) return;
+      int b, mt2, nt;
+      pair_tile_coords(f_tile, args, b, mt2, nt);
+      const int rt_a = mt2 * 2 + static_cast<int>(rank);
+      const int64_t arow = static_cast<int64_t>(b) * args.KT;
+      f_has_a = rt_a < args.RTA;
+      f_has_w1 = 2 * nt + 1 < args.RTB;
+      f_a = args.sfa + (arow * args.RTA + (f_has_a ? rt_a : 0)) * kAtomBytes + lane * 16;
+      f_w = args.sfb + (arow * args.RTB + 2 * nt) * kAtomBytes + lane * 16;
+    };
+    start_tile();
+    auto fetch = [&](uint4& va, uint4& vb0, uint4& vb1) {
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      va = f_has_a ? __ldg(reinterpret_cast<const uint4*>(f_a)) : zero;
+      vb0 = __ldg(reinterpret_cast<const uint4*>(f_w));
+      vb1 = f_has_w1 ? __ldg(reinterpret_cast<const uint4*>(f_w + kAtomBytes)) : zero;
+      f_a += a_step;
+      f_w += w_step;
+      if (++f_kt == args.KT) {
+        f_kt = 0;
+        f_tile += npairs;
+        start_tile();
+      }
+    };
+    // Stages go in pairs (2i, 2i + 1), which share a round of the ring.  The
+    // MMAs finish in issue order, so once the second stage's previous MMAs
+    // are done (its empty barrier) both scale slots are free; one arrive on
+    // sf_ready[i] then publishes both.  A lone last stage waits on its own.
+    uint4 ra[2 * P_SF_AHEAD], rb0[2 * P_SF_AHEAD], rb1[2 * P_SF_AHEAD];
+#pragma unroll
+    for (int d = 0; d < 2 * P_SF_AHEAD; ++d)
+      if (d < total) fetch(ra[d], rb0[d], rb1[d]);
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = pair; tile < args.total_tiles; tile += npairs) {
-      int b, mt2, nt;
-      pair_tile_coords(tile, args, b, mt2, nt);
-      const bool has_sfa = mt2 * 2 + static_cast<int>(rank) < args.RTA;
-      const int nb_atoms = min(2, args.RTB - nt * 2);
-      bool ok = true;
-      for (int kt = 0; kt < args.KT; ++kt) {
-        if (!mbar_wait(&sf_full[stage], phase, abort_flag)) {
+    bool ok = true;
+    for (int64_t j0 = 0; ok && j0 < total; j0 += 2 * P_SF_AHEAD) {
+#pragma unroll
+      for (int d = 0; d < 2 * P_SF_AHEAD; d += 2) {
+        const int64_t j = j0 + d;
+        if (!ok || j >= total) break;
+        const bool two = j + 1 < total;
+        if (!mbar_wait(&empty[stage + (two ? 1 : 0)], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        const uint8_t* sfa = smem + P_OFF_SFA + stage * P_SFA_BYTES + lane * 16;
-        const uint8_t* sfb = smem + P_OFF_SFB + stage * P_SFB_BYTES + lane * 16;
-        const uint4 va = has_sfa ? *reinterpret_cast<const uint4*>(sfa) : make_uint4(0, 0, 0, 0);
-        tmem_st_32x32b_x4(lane_base + P_T_SFA + stage * 4, va.x, va.y, va.z, va.w);
-        // weight scales for all 256 columns, in column order: each CTA's half
-        // of the pair MMA reads them from its own tensor memory
+        tc_fence_after();  // the MMAs that read these scale slots are done
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint4 vb = j < nb_atoms ? *reinterpret_cast<const uint4*>(sfb + j * kAtomBytes)
-                                        : make_uint4(0, 0, 0, 0);
-          tmem_st_32x32b_x4(lane_base + P_T_SFB + stage * 8 + 4 * j, vb.x, vb.y, vb.z, vb.w);
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int sl = stage + h;
+          tmem_st_32x32b_x4(lane_base + P_T_SFA + sl * 4, ra[d + h].x, ra[d + h].y, ra[d + h].z, ra[d + h].w);
+          tmem_st_32x32b_x4(lane_base + P_T_SFB + sl * 8, rb0[d + h].x, rb0[d + h].y, rb0[d + h].z, rb0[d + h].w);
+          tmem_st_32x32b_x4(lane_base + P_T_SFB + sl * 8 + 4, rb1[d + h].x, rb1[d + h].y, rb1[d + h].z,
+                            rb1[d + h].w);
         }
         tmem_st_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (j + h + 2 * P_SF_AHEAD < total) fetch(ra[d + h], rb0[d + h], rb1[d + h]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(ready_base + static_cast<uint32_t>(stage * 8));
-        if (++stage == PSTAGES) {
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(&sf_ready[stage >> 1]);
+          else
+            mbar_arrive_remote(ready_even + static_cast<uint32_t>((stage >> 1) * 8));
+        }
+        stage += 2;
+        if (stage == PSTAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -287,7 +332,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     for (int tile = pair; tile < args.total_tiles; tile += npairs) {
       int b, mt2, nt;
       pair_tile_coords(tile, args, b, mt2, nt);
-      if (!mbar_wait_cluster(acc_full, acc_phase, abort_flag)) break;
+      if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
       uint32_t packed[P_EPI_COLS / 2];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + P_T_ACC + col0;
@@ -321,7 +366,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_even);  // the even CTA may start the next tile
+      if (lane == 0) mbar_arrive_remote(acc_empty_even);  // the even CTA may start the next tile
       acc_phase ^= 1u;
 
       const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;

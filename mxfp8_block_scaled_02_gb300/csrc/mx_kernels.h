@@ -28,7 +28,7 @@ struct GemmProblem {
   const void* bias;  // bf16 [N] or nullptr
   void* out;         // bf16 [B, M, N]
   int64_t B, M, N, K;
-  int tiles = 0;     // 0 or 1: one CTA per 128 x 256 tile; 2: 256 x 256 tiles on CTA pairs
+  int tiles = 0;     // 0: by M (CTA pairs when M > 128); 1: one CTA per 128 x 256 tile; 2: CTA pairs
 };
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);

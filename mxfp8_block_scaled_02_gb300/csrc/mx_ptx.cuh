@@ -60,29 +60,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-suspending test with cluster-scope acquire, for barriers that other CTAs
-// of the cluster arrive on: a thread suspended in try_wait is not woken
-// promptly by an arrival from another CTA, so these waits poll instead.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Arrive with an expected transaction count on a barrier of another CTA of
-// the cluster (`addr` from map_shared_rank).
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(addr),
-               "r"(bytes)
-               : "memory");
-}
-
 // TMA load into this CTA's shared memory that completes on a barrier of either
 // CTA of the pair (cta_group::2 form; `bar_addr` from map_shared_rank).
 __device__ __forceinline__ void tma_load_3d_cluster_bar(void* dst, const CUtensorMap* m, uint32_t bar_addr,
@@ -94,10 +71,13 @@ __device__ __forceinline__ void tma_load_3d_cluster_bar(void* dst, const CUtenso
       : "memory");
 }
 
-// Arrive (release, cluster scope) on the barrier at `addr` in CTA space of
-// the cluster (from map_shared_rank).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// Arrive on the barrier at `addr` in another CTA of the cluster (from
+// map_shared_rank), with the default semantics (release at CTA scope).  The
+// hand-offs that use it order tensor-memory or async-proxy work the sender has
+// already waited for, so no cluster-scope fence is needed; a .release.cluster
+// arrive stalls the sending thread for most of a microsecond.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // Wait for the phase with parity `parity` to complete, for at most
@@ -121,28 +101,6 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort);
-}
-
-static __device__ __noinline__ bool mbar_wait_cluster_slow(uint64_t* bar, uint32_t parity,
-                                                           volatile int* abort) {
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (abort != nullptr && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      atomicOr(&g_status, kStatusTimeout);
-      if (abort != nullptr) *abort = 1;
-      return false;
-    }
-  }
-}
-
-// Bounded wait with cluster-scope acquire (see mbar_wait).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  return mbar_wait_cluster_slow(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------- TMA / bulk
