@@ -28,9 +28,13 @@
 //     the previous kernel in the stream writes, start before
 //     griddepcontrol.wait; reading x and writing out come after it, so
 //     consecutive layers overlap one's tail with the next one's weight stream.
-// Two shapes of the kernel: up to 16 tokens (4-stage ring, ~86 KB of shared
-// memory, two CTAs per SM so that the next call's CTAs fit beside this one's)
-// and up to 64 tokens (6-stage ring, one CTA per SM).
+//   * x has a ring of its own (8 K tiles), apart from the weight ring: with
+//     shared slots, quantising the second half of a CTA's K slice had to wait
+//     for the MMAs of the first half, a round trip on every call's critical
+//     path (dependency wait -> x -> MMAs -> reduction).
+// Two shapes of the kernel: up to 16 tokens (4-stage weight ring, ~95 KB of
+// shared memory, two CTAs per SM so that the next call's CTAs fit beside this
+// one's) and up to 64 tokens (6-stage weight ring, one CTA per SM).
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
 // and MMA issuer, 2..9 = activation quantiser, then (2..5) TMEM -> remote
 // shared memory and (2..9) the reduction.
@@ -55,21 +59,23 @@ constexpr int QTHREADS = 256;  // warps 2..9
 constexpr int THREADS = 64 + QTHREADS;
 constexpr int kWBytes = kRows * kTK;  // 16 KB
 
-template <int MAXTOK_, int STAGES_, int QLOADS_, int MINB_>
+template <int MAXTOK_, int STAGES_, int XSTAGES_, int QLOADS_, int MINB_>
 struct DCfg {
   static constexpr int MAXTOK = MAXTOK_;
-  static constexpr int STAGES = STAGES_;
+  static constexpr int STAGES = STAGES_;    // weight ring
+  static constexpr int XSTAGES = XSTAGES_;  // activation ring (its own slots and barriers)
   static constexpr int QLOADS = QLOADS_;  // 16-byte x loads per quantiser thread per group
   static constexpr int MINB = MINB_;      // CTAs per SM the kernel is built for
   static constexpr int XBYTES = MAXTOK * kTK;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_X = OFF_W + STAGES * kWBytes;
-  static constexpr int OFF_SFW = OFF_X + STAGES * XBYTES;
+  static constexpr int OFF_SFW = OFF_X + XSTAGES * XBYTES;
   static constexpr int OFF_SFX = OFF_SFW + STAGES * kAtomBytes;
-  static constexpr int OFF_RECV = OFF_SFX + STAGES * kAtomBytes;  // [S][n_mma][128/S] fp32
+  static constexpr int OFF_RECV = OFF_SFX + XSTAGES * kAtomBytes;  // [S][n_mma][128/S] fp32
   static constexpr int RECV_BYTES = MAXTOK * kRows * 4;
   static constexpr int OFF_BAR = OFF_RECV + RECV_BYTES;
-  static constexpr int NUM_BARS = 3 * STAGES + 1;  // full_w, full_x, empty per stage; acc_full
+  // full_w, empty per weight stage; full_x, x_empty per activation slot; acc_full
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * XSTAGES + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
@@ -83,8 +89,11 @@ struct DCfg {
   static_assert(QTHREADS % kRows == 0, "each reduction thread owns one output column");
 };
 
-using SmallCfg = DCfg<16, 4, 4, 2>;
-using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 1>;
+// Eight activation slots: at N = K = 4096 each CTA's K slice is 8 tiles at
+// S = 4, so all of x is quantised in one pass right after the dependency wait
+// instead of waiting for the MMAs of earlier tiles to free shared slots.
+using SmallCfg = DCfg<16, 4, 8, 4, 2>;
+using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 8, 1>;
 
 struct Args {
   const uint4* x;  // bf16 [M, K] as 16-byte chunks
@@ -112,9 +121,10 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full_w = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* full_x = full_w + C::STAGES;
-  uint64_t* empty = full_x + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* empty = full_w + C::STAGES;
+  uint64_t* full_x = empty + C::STAGES;
+  uint64_t* x_empty = full_x + C::XSTAGES;
+  uint64_t* acc_full = x_empty + C::XSTAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -129,8 +139,11 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full_w[s], 1);
-      mbar_init(&full_x[s], QTHREADS);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < C::XSTAGES; ++s) {
+      mbar_init(&full_x[s], QTHREADS);
+      mbar_init(&x_empty[s], 1);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -160,7 +173,15 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
                   a.sfw + (static_cast<int64_t>(kt0 + i) * a.RTW + tile) * kAtomBytes, kAtomBytes,
                   &full_w[st]);
         ++issued;
-        if (i + 1 == min(nk, C::STAGES)) launch_dependents();  // the next kernel may start loading
+        if (i + 1 == min(nk, C::STAGES)) {
+          launch_dependents();  // the next kernel may start loading
+          // The rest of the slice waits for ring slots that the MMAs free only
+          // after x is ready; ask L2 for it now.
+          for (int j = C::STAGES; j < nk; ++j) {
+            prefetch_tile_l2(&tmW, (kt0 + j) * kTK, tile * kRows, 0);
+            prefetch_bulk_l2(a.sfw + (static_cast<int64_t>(kt0 + j) * a.RTW + tile) * kAtomBytes, kAtomBytes);
+          }
+        }
       }
       if (*abort_flag) {
         for (int s = 0; s < C::STAGES && s < issued; ++s) {
@@ -178,22 +199,27 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       for (int i = 0; i < nk && ok; ++i) {
         const int st = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
-        if (!mbar_wait(&full_w[st], ph, abort_flag) || !mbar_wait(&full_x[st], ph, abort_flag)) {
+        const int xs = i % C::XSTAGES;
+        const uint32_t xph = (i / C::XSTAGES) & 1;
+        if (!mbar_wait(&full_w[st], ph, abort_flag) || !mbar_wait(&full_x[xs], xph, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        // TMEM scale slots follow the weight stage: the copies run on the
+        // tensor pipe in order behind the MMAs that read the slot before.
         const uint32_t t_sfw = tmem + C::T_SFW + st * 4;
         const uint32_t t_sfx = tmem + C::T_SFX + st * 4;
         tc_cp_sf(t_sfw, sdesc_sf(smem_u32(smem + C::OFF_SFW + st * kAtomBytes)));
-        tc_cp_sf(t_sfx, sdesc_sf(smem_u32(smem + C::OFF_SFX + st * kAtomBytes)));
+        tc_cp_sf(t_sfx, sdesc_sf(smem_u32(smem + C::OFF_SFX + xs * kAtomBytes)));
         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_W + st * kWBytes));
-        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_X + st * C::XBYTES));
+        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_X + xs * C::XBYTES));
 #pragma unroll
         for (int kk = 0; kk < kTK / 32; ++kk)
           tc_mma_mxf8(tmem + C::T_ACC, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk), t_sfw,
                       t_sfx, (i | kk) != 0);
         tc_commit(&empty[st]);
+        tc_commit(&x_empty[xs]);
       }
       if (ok) tc_commit(acc_full);
       else __nanosleep(200000);  // let issued tensor-core work retire
@@ -209,9 +235,9 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     const int t = threadIdx.x - 64;
     const int pt_shift = 31 - __clz(a.n_mma * 16);  // n_mma is a power of two
     const int per_tile = 1 << pt_shift;
-    // A group's ring slots must all be free at once while the MMA still owns
-    // the others, so a group spans at most half the ring.
-    const int G = max(1, min(C::STAGES / 2, (QTHREADS * C::QLOADS) >> pt_shift));
+    // A group's slots must all be free at once while the MMA still owns the
+    // others, so a group spans at most half the activation ring.
+    const int G = max(1, min(C::XSTAGES / 2, (QTHREADS * C::QLOADS) >> pt_shift));
     const int per_group = G * per_tile;  // a multiple of QTHREADS: whole warps
     auto load_group = [&](int g, uint4 (&dst)[C::QLOADS]) {
 #pragma unroll
@@ -228,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     // Wait for the group's ring slots, quantise it into them, signal the MMA.
     auto quantize_group = [&](int g, const uint4 (&cur)[C::QLOADS]) -> bool {
       for (int i = g * G; i < min(nk, (g + 1) * G); ++i)
-        if (!mbar_wait(&empty[i % C::STAGES], ((i / C::STAGES) & 1) ^ 1u, abort_flag)) return false;
+        if (!mbar_wait(&x_empty[i % C::XSTAGES], ((i / C::XSTAGES) & 1) ^ 1u, abort_flag)) return false;
 #pragma unroll
       for (int j = 0; j < C::QLOADS; ++j) {
         const int task = t + j * QTHREADS;
@@ -238,9 +264,9 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         uint2 codes;
         const uint32_t sbyte = quantize_quarter_block(cur[j], codes);  // all lanes take part
         if (task < per_group && i < nk) {
-          const int st = i % C::STAGES;
-          uint8_t* xt = smem + C::OFF_X + st * C::XBYTES;
-          uint8_t* sft = smem + C::OFF_SFX + st * kAtomBytes;
+          const int xs = i % C::XSTAGES;
+          uint8_t* xt = smem + C::OFF_X + xs * C::XBYTES;
+          uint8_t* sft = smem + C::OFF_SFX + xs * kAtomBytes;
           // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
           const int chunk = qd >> 1;
           *reinterpret_cast<uint2*>(xt + row * 128 + ((chunk ^ (row & 7)) << 4) + (qd & 1) * 8) = codes;
@@ -249,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         }
       }
       fence_proxy_async_smem();
-      for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::STAGES]);
+      for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
       return true;
     };
     const int ngroups = (nk + G - 1) / G;

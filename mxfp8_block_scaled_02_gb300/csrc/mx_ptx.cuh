@@ -108,6 +108,18 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
 
+// Ask L2 to fetch a 3-D box of a tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void prefetch_tile_l2(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m), "r"(c0),
+               "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_bulk_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
                                             int c1, int c2) {
   asm volatile(
