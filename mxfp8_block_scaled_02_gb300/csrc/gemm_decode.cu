@@ -32,9 +32,8 @@
 //     shared slots, quantising the second half of a CTA's K slice had to wait
 //     for the MMAs of the first half, a round trip on every call's critical
 //     path (dependency wait -> x -> MMAs -> reduction).
-// Two shapes of the kernel: up to 16 tokens (4-stage weight ring, ~95 KB of
-// shared memory, two CTAs per SM so that the next call's CTAs fit beside this
-// one's) and up to 64 tokens (6-stage weight ring, one CTA per SM).
+// Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~160 KB of
+// shared memory) and up to 64 tokens (6-stage weight ring), one CTA per SM.
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
 // and MMA issuer, 2..9 = activation quantiser, then (2..5) TMEM -> remote
 // shared memory and (2..9) the reduction.
@@ -91,8 +90,11 @@ struct DCfg {
 
 // Eight activation slots: at N = K = 4096 each CTA's K slice is 8 tiles at
 // S = 4, so all of x is quantised in one pass right after the dependency wait
-// instead of waiting for the MMAs of earlier tiles to free shared slots.
-using SmallCfg = DCfg<16, 4, 8, 4, 2>;
+// instead of waiting for the MMAs of earlier tiles to free shared slots.  Up to
+// 16 tokens the weight ring holds the whole 8-tile slice too (one CTA per SM):
+// measured 8.45 us per call at M = 1 against 9.10 us for a 4-stage ring at two
+// CTAs per SM, whose second half of the slice refilled on the critical path.
+using SmallCfg = DCfg<16, 8, 8, 4, 1>;
 using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 8, 1>;
 
 struct Args {
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < C::XSTAGES; ++s) {
-      mbar_init(&full_x[s], QTHREADS);
+      mbar_init(&full_x[s], QTHREADS / 32);  // one arrive per quantiser warp
       mbar_init(&x_empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -275,7 +277,11 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         }
       }
       fence_proxy_async_smem();
-      for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
+      // One arrive per warp: arrivals on a barrier are serialised, and 256 per
+      // K tile made the tiles ready one by one, ~0.3 us apart.
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0)
+        for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
       return true;
     };
     const int ngroups = (nk + G - 1) / G;
