@@ -229,6 +229,23 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     __syncwarp();
   } else {
     // x is written by the previous kernel in the stream: wait for it to finish.
+    // Token rows M .. n_mma - 1 are zero in every K tile: write their codes and
+    // scale bytes once, before the dependency wait, and quantise only rows < M
+    // afterwards (a zero block quantises to byte 0 and zero codes, so this is
+    // what quantising them would write).  Rows < M are never touched here.
+    {
+      const int tz = threadIdx.x - 64;
+      const int zrows = a.n_mma - a.M;
+      for (int idx = tz; idx < C::XSTAGES * zrows * 8; idx += QTHREADS) {
+        const int xs = idx / (zrows * 8);
+        const int rem = idx - xs * zrows * 8;
+        const int row = a.M + rem / 8;
+        *reinterpret_cast<uint4*>(smem + C::OFF_X + xs * C::XBYTES + row * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+        if ((rem & 7) == 0)
+          *reinterpret_cast<uint32_t*>(smem + C::OFF_SFX + xs * kAtomBytes + (row & 31) * 16 + (row >> 5) * 4) = 0u;
+      }
+    }
     grid_dependency_wait();
     // ------------------------------------------------ activation quantiser
     // A task is one 16-byte chunk (8 bf16) of x: k tile i, row r < n_mma,
@@ -263,6 +280,8 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         const int i = g * G + (task >> pt_shift);
         const int rem = task & (per_tile - 1);
         const int row = rem >> 4, qd = rem & 15;
+        // a warp covers two token rows (16 chunks each); rows >= M were zeroed
+        if ((((task & ~31) & (per_tile - 1)) >> 4) >= a.M) continue;
         uint2 codes;
         const uint32_t sbyte = quantize_quarter_block(cur[j], codes);  // all lanes take part
         if (task < per_group && i < nk) {
