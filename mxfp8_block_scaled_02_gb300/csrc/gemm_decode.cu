@@ -35,10 +35,8 @@
 // Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~160 KB of
 // shared memory) and up to 64 tokens (6-stage weight ring), one CTA per SM.
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
-// and MMA issuer, 2..9 = activation quantiser, (2..5) also the scale writers
-// (tcgen05.st of both scale atoms of each K tile, so the tensor pipe runs
-// only MMAs), then (2..5) TMEM -> remote shared memory and (2..9) the
-// reduction.
+// and MMA issuer, 2..9 = activation quantiser, then (2..5) TMEM -> remote
+// shared memory and (2..9) the reduction.
 // Every mbarrier wait is bounded; the cluster barrier is reached on every
 // path, also after an expired wait.
 #include <cuda_bf16.h>
@@ -210,10 +208,12 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
           break;
         }
         tc_fence_after();
-        // Both scale slots of the stage were written by warps 2..5 before
-        // they arrived on full_x (tcgen05.st, off the tensor pipe).
+        // TMEM scale slots follow the weight stage: the copies run on the
+        // tensor pipe in order behind the MMAs that read the slot before.
         const uint32_t t_sfw = tmem + C::T_SFW + st * 4;
         const uint32_t t_sfx = tmem + C::T_SFX + st * 4;
+        tc_cp_sf(t_sfw, sdesc_sf(smem_u32(smem + C::OFF_SFW + st * kAtomBytes)));
+        tc_cp_sf(t_sfx, sdesc_sf(smem_u32(smem + C::OFF_SFX + xs * kAtomBytes)));
         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_W + st * kWBytes));
         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_X + xs * C::XBYTES));
 #pragma unroll
@@ -270,20 +270,12 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
                      : make_uint4(0, 0, 0, 0);
       }
     };
-    // Wait for the group's ring slots, quantise it into them, move the scales
-    // of its K tiles into tensor memory, signal the MMA.  Every quantiser warp
-    // runs every group to the named barrier, also after an expired wait (the
-    // barrier has no timeout), and only then skips the rest.
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    auto quantize_group = [&](int g, const uint4 (&cur)[C::QLOADS]) {
-      const int i_end = min(nk, (g + 1) * G);
-      bool ok = !*abort_flag;
-      for (int i = g * G; ok && i < i_end; ++i)
-        ok = mbar_wait(&x_empty[i % C::XSTAGES], ((i / C::XSTAGES) & 1) ^ 1u, abort_flag);
-      ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform: the quantiser shuffles within the warp
+    // Wait for the group's ring slots, quantise it into them, signal the MMA.
+    auto quantize_group = [&](int g, const uint4 (&cur)[C::QLOADS]) -> bool {
+      for (int i = g * G; i < min(nk, (g + 1) * G); ++i)
+        if (!mbar_wait(&x_empty[i % C::XSTAGES], ((i / C::XSTAGES) & 1) ^ 1u, abort_flag)) return false;
 #pragma unroll
       for (int j = 0; j < C::QLOADS; ++j) {
-        if (!ok) break;
         const int task = t + j * QTHREADS;
         const int i = g * G + (task >> pt_shift);
         const int rem = task & (per_tile - 1);
@@ -304,40 +296,22 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, QTHREADS);  // the group's scale bytes are all in shared memory
-      // Warps 2..5 (one per TMEM lane quarter) write each K tile's weight and
-      // activation scale atoms into the stage's TMEM slots: one 16-byte atom
-      // line per lane.  The weight stage must have landed; its arrival also
-      // means the MMAs that read these slots before have finished.
-      if (warp < 6) {
-        for (int i = g * G; ok && i < i_end; ++i) {
-          const int st = i % C::STAGES;
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full_w[st], (i / C::STAGES) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const uint4 vw = *reinterpret_cast<const uint4*>(smem + C::OFF_SFW + st * kAtomBytes + lane * 16);
-          const uint4 vx =
-              *reinterpret_cast<const uint4*>(smem + C::OFF_SFX + (i % C::XSTAGES) * kAtomBytes + lane * 16);
-          tmem_st_32x32b_x4(lane_base + C::T_SFW + st * 4, vw.x, vw.y, vw.z, vw.w);
-          tmem_st_32x32b_x4(lane_base + C::T_SFX + st * 4, vx.x, vx.y, vx.z, vx.w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-      }
-      // One arrive per warp: arrivals on a barrier are serialised.
+      // One arrive per warp: arrivals on a barrier are serialised, and 256 per
+      // K tile made the tiles ready one by one, ~0.3 us apart.
       __syncwarp();
-      if (ok && lane == 0)
-        for (int i = g * G; i < i_end; ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
+      if ((threadIdx.x & 31) == 0)
+        for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
+      return true;
     };
     const int ngroups = (nk + G - 1) / G;
     uint4 buf0[C::QLOADS], buf1[C::QLOADS];  // two register sets: load one group ahead
     load_group(0, buf0);
-    for (int g = 0; g < ngroups; g += 2) {  // every warp runs every group (named barrier)
+    for (int g = 0; g < ngroups; g += 2) {
       if (g + 1 < ngroups) load_group(g + 1, buf1);
-      quantize_group(g, buf0);
+      if (!quantize_group(g, buf0)) break;
       if (g + 1 >= ngroups) break;
       if (g + 2 < ngroups) load_group(g + 2, buf0);
-      quantize_group(g + 1, buf1);
+      if (!quantize_group(g + 1, buf1)) break;
     }
 
     // ------------------------------------------------ epilogue: TMEM -> owner's receive buffer

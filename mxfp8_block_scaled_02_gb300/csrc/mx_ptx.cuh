@@ -330,12 +330,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, u
                : "memory");
 }
 
-// Named barrier `id` (1..15) over `count` threads (a multiple of 32).  Every
-// participating thread must reach it on every path: it has no timeout.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
