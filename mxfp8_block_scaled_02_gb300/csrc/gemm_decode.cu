@@ -109,14 +109,6 @@ struct Args {
   int splits;  // cluster size S
 };
 
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 template <class C>
 __global__ void __launch_bounds__(THREADS, C::MINB)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const Args a) {

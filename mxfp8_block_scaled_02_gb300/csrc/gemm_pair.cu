@@ -143,6 +143,33 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Prologue for the first ring round (all slots free): the weight tiles
+      // do not depend on the kernel before this one in the stream, the
+      // activation tiles (its output) do.  Issue the weights, wait for the
+      // dependency (programmatic dependent launch), then the activations.
+      const int my_tiles = pair < args.total_tiles ? (args.total_tiles - 1 - pair) / npairs + 1 : 0;
+      const int P0 = static_cast<int>(min(static_cast<int64_t>(PSTAGES), static_cast<int64_t>(my_tiles) * args.KT));
+      for (int pass = 0; pass < 2; ++pass) {
+        int tile = pair, kt = 0, b = 0, mt2 = 0, nt = 0;
+        if (P0 > 0) pair_tile_coords(tile, args, b, mt2, nt);
+        for (int s0 = 0; s0 < P0; ++s0) {
+          const uint32_t full_even = map_shared_rank(smem_u32(&full[s0]), 0);
+          if (pass == 0) {
+            if (leader) mbar_arrive_expect_tx(&full[s0], 2 * (P_A_BYTES + P_B_BYTES));
+            tma_load_3d_cluster_bar(smem + P_OFF_B + s0 * P_B_BYTES, &tmB, full_even, kt * PBK,
+                                    nt * PBN + static_cast<int>(rank) * (PBN / 2), b);
+          } else {
+            tma_load_3d_cluster_bar(smem + P_OFF_A + s0 * P_A_BYTES, &tmA, full_even, kt * PBK,
+                                    (mt2 * 2 + static_cast<int>(rank)) * PBM, b);
+          }
+          if (++kt == args.KT) {
+            kt = 0;
+            tile += npairs;
+            if (tile < args.total_tiles) pair_tile_coords(tile, args, b, mt2, nt);
+          }
+        }
+        if (pass == 0) grid_dependency_wait();
+      }
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -152,6 +179,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         pair_tile_coords(tile, args, b, mt2, nt);
         const int rt_a = mt2 * 2 + static_cast<int>(rank);  // this CTA's activation row tile
         for (int kt = 0; kt < args.KT; ++kt) {
+          if (issued < P0) {  // issued by the prologue
+            ++issued;
+            if (++stage == PSTAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -234,6 +269,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     // write waits for the stage's previous MMAs (empty barrier).
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t ready_even = map_shared_rank(smem_u32(sf_ready), 0);
+    grid_dependency_wait();  // the activation scales are the previous kernel's output
     const int my_tiles = pair < args.total_tiles ? (args.total_tiles - 1 - pair) / npairs + 1 : 0;
     const int64_t total = static_cast<int64_t>(my_tiles) * args.KT;
     // Fetch cursor: pointers to this lane's line of the activation atom and
@@ -445,13 +481,17 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   cfg.blockDim = dim3(P_THREADS, 1, 1);
   cfg.dynamicSmemBytes = P_SMEM_ALLOC;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the prologue and the first weight tiles
+  // overlap the end of the kernel before (normally the quantiser)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, a);
   if (e != cudaSuccess) *msg = "pair GEMM launch failed";
   return e;

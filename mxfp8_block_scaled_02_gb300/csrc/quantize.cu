@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     const uint4* __restrict__ x, uint32_t KB, uint32_t tasks_per_row, uint32_t items_per_row,
     uint32_t nitems, uint8_t* __restrict__ q, uint8_t* __restrict__ s, uint32_t rows_per_b,
     uint32_t RT, uint32_t KT) {
+  // The GEMM that follows may start its prologue and weight loads now; it
+  // waits for this grid to finish before it reads the codes and scales.
+  launch_dependents();
   const int lane = threadIdx.x & 31;
   const uint32_t j = lane >> 2, part = lane & 3;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
