@@ -1,7 +1,9 @@
 // quantize.cu - dynamic MXFP8 quantisation and the scale-factor repack.
 //
-// The per-block arithmetic (OCP MX v1.0, section 6.3) lives in mx_quant.cuh,
-// shared with the fused small-M GEMM so that both produce the same bytes.
+// The per-block arithmetic (OCP MX v1.0, section 6.3) lives in mx_quant.cuh:
+// this kernel uses quantize_block32 (one lane per block), the fused small-M
+// GEMM quantize_quarter_block (four lanes per block); both take the same
+// decisions on the same bf16 bits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -16,80 +18,60 @@ namespace mx {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;  // 8-block tasks per work item, loads all in flight
+constexpr int kQU = 2;  // 32-block warp tasks per loop iteration, loads all in flight
 
-// A task is 8 consecutive 32-element blocks of one row (256 values, 512
-// bytes of bf16); lane l owns 8 values: block j = l / 4 of the task, quarter
-// l % 4 of that block, and four lanes combine their amax by shuffles.  A work
-// item is kQuantUnroll consecutive tasks of one row, so the row (and, for the
-// packed layout, its batch and atom row) is found with one division per item.
-// kPacked selects the scale output: false = row-major [rows, K/32], true = the
-// 512-byte atom layout of mx_layout.cuh (rows grouped per batch of rows_per_b).
+// Block g of the flat [rows, K] array is row g / KB, block g % KB; its codes
+// are bytes [32 g, 32 g + 32) of q and, in the row-major scale layout, its
+// scale is byte g of s.  Lane l of a warp task takes block 32 t + l, so a warp
+// reads 2 KB and writes 1 KB of codes and 32 scale bytes, contiguous.
+// kPacked selects the 512-byte atom layout of mx_layout.cuh for the scales
+// (rows grouped per batch of rows_per_b).
 template <bool kPacked>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
-    const uint4* __restrict__ x, uint32_t KB, uint32_t tasks_per_row, uint32_t items_per_row,
-    uint32_t nitems, uint8_t* __restrict__ q, uint8_t* __restrict__ s, uint32_t rows_per_b,
-    uint32_t RT, uint32_t KT) {
+    const uint4* __restrict__ x, uint32_t total_blocks, uint32_t KB, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT, uint32_t KT) {
   // The GEMM that follows may start its prologue and weight loads now; it
   // waits for this grid to finish before it reads the codes and scales.
   launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const uint32_t j = lane >> 2, part = lane & 3;
+  const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t ntasks = (total_blocks + 31) / 32;
   const int64_t atom_k_stride = static_cast<int64_t>(RT) * kAtomBytes;  // next K tile, same rows
 
-  for (uint32_t item = warp; item < nitems; item += nwarps) {
-    const uint32_t row = item / items_per_row;
-    const uint32_t t0 = (item - row * items_per_row) * kQuantUnroll;
-    const int64_t row_blk = static_cast<int64_t>(row) * KB;  // first block of the row
-    uint4 v[kQuantUnroll];
+  for (uint32_t t0 = warp * kQU; t0 < ntasks; t0 += nwarps * kQU) {
+    uint4 v[kQU][4];
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t kb = (t0 + u) * 8 + j;
-      const bool valid = t0 + u < tasks_per_row && kb < KB;
-      v[u] = valid ? __ldg(x + (row_blk + kb) * 4 + part) : make_uint4(0, 0, 0, 0);
-    }
-    int64_t atom_row = 0;  // packed: offset of (row, block 0) in its first atom
-    if (kPacked) {
-      const uint32_t b = row / rows_per_b, r = row - b * rows_per_b;
-      atom_row = (static_cast<int64_t>(b) * KT * RT + (r >> 7)) * kAtomBytes + (r & 31) * 16 +
-                 ((r >> 5) & 3) * 4;
+    for (int u = 0; u < kQU; ++u) {
+      const uint32_t g = (t0 + u) * 32 + lane;
+      const bool valid = t0 + u < ntasks && g < total_blocks;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[u][k] = valid ? __ldg(x + static_cast<uint64_t>(g) * 4 + k) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t task = t0 + u;
-      const uint32_t kb_task = task * 8;
-      const uint32_t kb = kb_task + j;
-      const bool valid = task < tasks_per_row && kb < KB;
-      uint2 codes;
-      const uint32_t sbyte = quantize_quarter_block(v[u], codes);
-      if (valid) *reinterpret_cast<uint2*>(q + (row_blk + kb) * 32 + part * 8) = codes;
-
-      // Scale bytes: gather the task's 8 bytes (lanes 0, 4, ..., 28) so that
-      // whole words are stored when the task is complete.
-      const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 0);
-      const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 4);
-      const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 8);
-      const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, sbyte, (lane & 16) + 12);
-      const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-      const bool full_task = task < tasks_per_row && kb_task + 8 <= KB;
-      if (kPacked) {
-        // blocks kb..kb+3 (kb % 4 == 0) are 4 consecutive bytes of one atom
-        if (full_task) {
-          if ((lane & 15) == 0)
-            *reinterpret_cast<uint32_t*>(s + atom_row + (kb >> 2) * atom_k_stride) = word;
-        } else if (valid && part == 0) {
-          s[atom_row + (kb >> 2) * atom_k_stride + (kb & 3)] = static_cast<uint8_t>(sbyte);
-        }
+    for (int u = 0; u < kQU; ++u) {
+      const uint32_t g0 = (t0 + u) * 32;
+      const uint32_t g = g0 + lane;
+      uint4 c0, c1;
+      const uint32_t sbyte = quantize_block32(v[u], c0, c1);
+      if (t0 + u >= ntasks || g >= total_blocks) continue;
+      uint4* qd = reinterpret_cast<uint4*>(q + static_cast<uint64_t>(g) * 32);
+      qd[0] = c0;
+      qd[1] = c1;
+      if (!kPacked) {
+        s[g] = static_cast<uint8_t>(sbyte);
       } else {
-        const uint32_t hi_word = __shfl_sync(0xFFFFFFFFu, word, 16);
-        const int64_t off = row_blk + kb_task;
-        if (full_task && (off & 7) == 0) {
-          if (lane == 0) *reinterpret_cast<uint2*>(s + off) = make_uint2(word, hi_word);
-        } else if (valid && part == 0) {
-          s[row_blk + kb] = static_cast<uint8_t>(sbyte);
+        // row and block of the warp's first block (one division), then this lane's
+        uint32_t row = g0 / KB;
+        uint32_t kb = g0 - row * KB + lane;
+        while (kb >= KB) {
+          kb -= KB;
+          ++row;
         }
+        const uint32_t b = row / rows_per_b, r = row - b * rows_per_b;
+        s[(static_cast<int64_t>(b) * KT * RT + (r >> 7)) * kAtomBytes + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
+          (kb >> 2) * atom_k_stride + (kb & 3)] = static_cast<uint8_t>(sbyte);
       }
     }
   }
@@ -152,11 +134,9 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
                             cudaStream_t stream) {
   (void)B;
   const int64_t KB = K / 32;
-  const int64_t tasks_per_row = ceil_div(KB, 8);
-  const int64_t items_per_row = ceil_div(tasks_per_row, kQuantUnroll);
-  const int64_t nitems = rows * items_per_row;
-  if (nitems == 0) return cudaSuccess;
-  if (nitems > 0x7FFFFFFFll || KB > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  const int64_t total_blocks = rows * KB;
+  if (total_blocks == 0) return cudaSuccess;
+  if (total_blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
   static int per_sm[2] = {0, 0};
   int& occ = per_sm[packed_scales ? 1 : 0];
   if (occ == 0) {
@@ -165,18 +145,17 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<false>, kQuantThreads, 0);
     if (e != cudaSuccess || occ < 1) occ = 1;
   }
-  const int grid = grid_for(nitems * 32, kQuantThreads, sms, occ);
+  const int64_t ntasks = ceil_div(total_blocks, 32);
+  const int grid = grid_for(ceil_div(ntasks, kQU) * 32, kQuantThreads, sms, occ);
   const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
   const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
   if (packed_scales)
     quantize_kernel<true><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
-        static_cast<uint32_t>(items_per_row), static_cast<uint32_t>(nitems), q, s,
+        static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(KB), q, s,
         static_cast<uint32_t>(rows_per_b), RT, KT);
   else
     quantize_kernel<false><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<uint32_t>(KB), static_cast<uint32_t>(tasks_per_row),
-        static_cast<uint32_t>(items_per_row), static_cast<uint32_t>(nitems), q, s,
+        static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(KB), q, s,
         static_cast<uint32_t>(rows_per_b), RT, KT);
   return cudaGetLastError();
 }
