@@ -141,6 +141,12 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
  *   to bf16 after the bias add.  Requirements: B >= 1, M >= 0 (0 is a no-op),
  *   N > 0 with N % 8 == 0, K > 0 with K % 128 == 0 (else MXFP8_ERR_UNSUPPORTED),
  *   all pointers 16-byte aligned.
+ *   Stream ordering: the GEMM kernels are launched with programmatic stream
+ *   serialization.  When the kernel before them in the stream triggers its
+ *   dependents early (griddepcontrol.launch_dependents), they may read
+ *   w_packed, sf_packed and bias before that kernel ends; x, x_q, x_scale
+ *   and out are touched only after it has finished.  Kernels launched the
+ *   ordinary way never trigger early, so for them this is plain stream order.
  */
 mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,
                           int64_t B, int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
