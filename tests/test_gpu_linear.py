@@ -306,10 +306,12 @@ def test_small_m_path_refuses_what_it_cannot_do():
 
 
 # ------------------------------------------------------------------ CTA-pair tiles at large M
-@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (300, 520, 512)])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (300, 520, 512), (260, 264, 128), (4096, 4096, 256)])
 def test_single_cta_tiles_exact_scales(M, N, K):
     """The large-M path on the exact scale-pattern problem with one CTA per
-    128 x 256 tile (path 2) and with 256 x 256 tiles on CTA pairs (path 3)."""
+    128 x 256 tile (path 2) and with 256 x 256 tiles on CTA pairs (path 3).
+    K = 128 is one K tile; at 4096 x 4096 x 256 each pair has several tiles of
+    two K tiles, so the pair kernel's first ring round spans tile boundaries."""
     KB = K // 32
     m = np.arange(M)[:, None]
     n = np.arange(N)[:, None]
