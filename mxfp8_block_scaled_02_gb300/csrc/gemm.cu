@@ -6,6 +6,8 @@
 // (aiter_flydsl page) followed by its bias add, with "Mxfp8LinearLayerConfig.
 // bmm_batch_size" as an extra grid dimension.
 //
+// Serves M <= 128 when the fused small-M path does not apply (path 2 forces
+// it); M > 128 goes to the CTA-pair kernel of gemm_pair.cu.
 // One persistent CTA per SM walks 128 x BN output tiles.  Warp roles:
 //   warp 0       TMA producer: A / W tiles (128-byte swizzle) and scale atoms
 //                into a STAGES-deep shared-memory ring; the atoms complete on

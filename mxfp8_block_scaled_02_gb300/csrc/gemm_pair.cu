@@ -10,7 +10,12 @@
 // its shared memory, and receives the 128 x 256 fp32 accumulator of its rows
 // in its tensor memory.  Per SM and K tile that is 16 KB of activations and
 // 16 KB of weights for the work that takes 16 + 32 KB with one CTA per tile,
-// which matters because the tensor cores outrun what one SM's TMA can load.
+// and one MMA instruction covers 256 rows: each block-scaled MMA has a large
+// fixed cost, so the widest shape per instruction is the fastest.
+//
+// The kernel is launched with programmatic stream serialization: the first
+// ring round of weight tiles is issued before griddepcontrol.wait, the
+// activation tiles and scales (the previous kernel's output) after it.
 //
 // Warp roles per CTA (both CTAs run every role but the MMA issuer):
 //   warp 0       TMA producer for this CTA's operand halves; both CTAs' copies
