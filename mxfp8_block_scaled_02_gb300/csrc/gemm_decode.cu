@@ -58,12 +58,12 @@ constexpr int QTHREADS = 256;  // warps 2..9
 constexpr int THREADS = 64 + QTHREADS;
 constexpr int kWBytes = kRows * kTK;  // 16 KB
 
-template <int MAXTOK_, int STAGES_, int XSTAGES_, int QLOADS_, int MINB_>
+template <int MAXTOK_, int STAGES_, int XSTAGES_, int QB_, int MINB_>
 struct DCfg {
   static constexpr int MAXTOK = MAXTOK_;
   static constexpr int STAGES = STAGES_;    // weight ring
   static constexpr int XSTAGES = XSTAGES_;  // activation ring (its own slots and barriers)
-  static constexpr int QLOADS = QLOADS_;  // 16-byte x loads per quantiser thread per group
+  static constexpr int QB = QB_;          // 32-element x blocks per quantiser thread per group
   static constexpr int MINB = MINB_;      // CTAs per SM the kernel is built for
   static constexpr int XBYTES = MAXTOK * kTK;
   static constexpr int OFF_W = 0;
@@ -94,8 +94,8 @@ struct DCfg {
 // 16 tokens the weight ring holds the whole 8-tile slice too (one CTA per SM):
 // measured 8.45 us per call at M = 1 against 9.10 us for a 4-stage ring at two
 // CTAs per SM, whose second half of the slice refilled on the critical path.
-using SmallCfg = DCfg<16, 8, 8, 4, 1>;
-using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 8, 1>;
+using SmallCfg = DCfg<16, 8, 8, 1, 1>;
+using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 2, 1>;
 
 struct Args {
   const uint4* x;  // bf16 [M, K] as 16-byte chunks
@@ -240,63 +240,62 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     }
     grid_dependency_wait();
     // ------------------------------------------------ activation quantiser
-    // A task is one 16-byte chunk (8 bf16) of x: k tile i, row r < n_mma,
-    // chunk qd < 16 of the row's 128 values.  One group = G k tiles =
-    // G * n_mma * 16 tasks, at most QLOADS per thread.
+    // A task is one 32-element block of x: K tile i, token row r < M, block j
+    // of the tile's four, one lane per block (quantize_block32, as in the
+    // standalone quantize kernel; a lane per quarter block with shuffles took
+    // ~7 us for 64 tokens).  One group = G K tiles = G * M * 4 tasks, at most
+    // QB per thread.  Rows M .. n_mma - 1 were zeroed above.
     const int t = threadIdx.x - 64;
-    const int pt_shift = 31 - __clz(a.n_mma * 16);  // n_mma is a power of two
-    const int per_tile = 1 << pt_shift;
+    const int per_tile = a.M * 4;
     // A group's slots must all be free at once while the MMA still owns the
     // others, so a group spans at most half the activation ring.
-    const int G = max(1, min(C::XSTAGES / 2, (QTHREADS * C::QLOADS) >> pt_shift));
-    const int per_group = G * per_tile;  // a multiple of QTHREADS: whole warps
-    auto load_group = [&](int g, uint4 (&dst)[C::QLOADS]) {
+    const int G = max(1, min(C::XSTAGES / 2, (QTHREADS * C::QB) / per_tile));
+    const int per_group = G * per_tile;  // <= QTHREADS * QB
+    auto load_group = [&](int g, uint4 (&dst)[C::QB][4]) {
 #pragma unroll
-      for (int j = 0; j < C::QLOADS; ++j) {
-        const int task = t + j * QTHREADS;
-        const int i = g * G + (task >> pt_shift);
-        const int rem = task & (per_tile - 1);
-        const int row = rem >> 4, qd = rem & 15;
-        dst[j] = (task < per_group && i < nk && row < a.M)
-                     ? __ldg(a.x + (static_cast<int64_t>(row) * a.K + (kt0 + i) * kTK) / 8 + qd)
-                     : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < C::QB; ++u) {
+        const int task = t + u * QTHREADS;
+        const int ti = task / per_tile;
+        const int i = g * G + ti;
+        const int rem = task - ti * per_tile;
+        const bool valid = task < per_group && i < nk;
+        const uint4* src =
+            a.x + (static_cast<int64_t>(rem >> 2) * a.K + (kt0 + i) * kTK + (rem & 3) * 32) / 8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[u][k] = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
       }
     };
     // Wait for the group's ring slots, quantise it into them, signal the MMA.
-    auto quantize_group = [&](int g, const uint4 (&cur)[C::QLOADS]) -> bool {
+    auto quantize_group = [&](int g, const uint4 (&cur)[C::QB][4]) -> bool {
       for (int i = g * G; i < min(nk, (g + 1) * G); ++i)
         if (!mbar_wait(&x_empty[i % C::XSTAGES], ((i / C::XSTAGES) & 1) ^ 1u, abort_flag)) return false;
 #pragma unroll
-      for (int j = 0; j < C::QLOADS; ++j) {
-        const int task = t + j * QTHREADS;
-        const int i = g * G + (task >> pt_shift);
-        const int rem = task & (per_tile - 1);
-        const int row = rem >> 4, qd = rem & 15;
-        // a warp covers two token rows (16 chunks each); rows >= M were zeroed
-        if ((((task & ~31) & (per_tile - 1)) >> 4) >= a.M) continue;
-        uint2 codes;
-        const uint32_t sbyte = quantize_quarter_block(cur[j], codes);  // all lanes take part
-        if (task < per_group && i < nk) {
-          const int xs = i % C::XSTAGES;
-          uint8_t* xt = smem + C::OFF_X + xs * C::XBYTES;
-          uint8_t* sft = smem + C::OFF_SFX + xs * kAtomBytes;
-          // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-          const int chunk = qd >> 1;
-          *reinterpret_cast<uint2*>(xt + row * 128 + ((chunk ^ (row & 7)) << 4) + (qd & 1) * 8) = codes;
-          if ((qd & 3) == 0)
-            sft[(row & 31) * 16 + (row >> 5) * 4 + (qd >> 2)] = static_cast<uint8_t>(sbyte);
-        }
+      for (int u = 0; u < C::QB; ++u) {
+        const int task = t + u * QTHREADS;
+        const int ti = task / per_tile;
+        const int i = g * G + ti;
+        if (task >= per_group || i >= nk) break;
+        const int rem = task - ti * per_tile;
+        const int row = rem >> 2, j = rem & 3;
+        uint4 c0, c1;
+        const uint32_t sbyte = quantize_block32(cur[u], c0, c1);
+        const int xs = i % C::XSTAGES;
+        uint8_t* xrow = smem + C::OFF_X + xs * C::XBYTES + row * 128;
+        // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8);
+        // block j is chunks 2j and 2j + 1 of its row
+        *reinterpret_cast<uint4*>(xrow + (((2 * j) ^ (row & 7)) << 4)) = c0;
+        *reinterpret_cast<uint4*>(xrow + (((2 * j + 1) ^ (row & 7)) << 4)) = c1;
+        smem[C::OFF_SFX + xs * kAtomBytes + (row & 31) * 16 + (row >> 5) * 4 + j] = static_cast<uint8_t>(sbyte);
       }
       fence_proxy_async_smem();
-      // One arrive per warp: arrivals on a barrier are serialised, and 256 per
-      // K tile made the tiles ready one by one, ~0.3 us apart.
+      // One arrive per warp: arrivals on a barrier are serialised.
       __syncwarp();
       if ((threadIdx.x & 31) == 0)
         for (int i = g * G; i < min(nk, (g + 1) * G); ++i) mbar_arrive(&full_x[i % C::XSTAGES]);
       return true;
     };
     const int ngroups = (nk + G - 1) / G;
-    uint4 buf0[C::QLOADS], buf1[C::QLOADS];  // two register sets: load one group ahead
+    uint4 buf0[C::QB][4], buf1[C::QB][4];  // two register sets: load one group ahead
     load_group(0, buf0);
     for (int g = 0; g < ngroups; g += 2) {
       if (g + 1 < ngroups) load_group(g + 1, buf1);
