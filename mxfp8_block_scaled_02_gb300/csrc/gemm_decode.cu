@@ -35,8 +35,11 @@
 // Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~160 KB of
 // shared memory) and up to 64 tokens (6-stage weight ring), one CTA per SM.
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
-// and MMA issuer, 2..9 = activation quantiser, then (2..5) TMEM -> remote
-// shared memory and (2..9) the reduction.
+// and MMA issuer for the even K tiles, 10 = MMA issuer for the odd K tiles
+// (each into its own accumulator; issuing a K tile's copies and MMAs takes one
+// thread ~400 cycles, so two issuers halve that part of the call), 2..9 =
+// activation quantiser, then (2..5) TMEM -> remote shared memory (the two
+// accumulators summed in fixed order) and (2..9) the reduction.
 // Every mbarrier wait is bounded; the cluster barrier is reached on every
 // path, also after an expired wait.
 #include <cuda_bf16.h>
@@ -55,7 +58,8 @@ namespace {
 constexpr int kRows = 128;  // weight rows per CTA = MMA M
 constexpr int kTK = 128;    // K elements per stage
 constexpr int QTHREADS = 256;  // warps 2..9
-constexpr int THREADS = 64 + QTHREADS;
+constexpr int kMma2Warp = 2 + QTHREADS / 32;  // second MMA issuer (odd K tiles)
+constexpr int THREADS = 64 + QTHREADS + 32;
 constexpr int kWBytes = kRows * kTK;  // 16 KB
 
 template <int MAXTOK_, int STAGES_, int XSTAGES_, int QB_, int MINB_>
@@ -78,12 +82,13 @@ struct DCfg {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
-  static constexpr int T_ACC = 0;  // MAXTOK fp32 columns
-  static constexpr int T_SFW = MAXTOK;
+  static constexpr int T_ACC = 0;        // MAXTOK fp32 columns: even K tiles
+  static constexpr int T_ACC1 = MAXTOK;  // odd K tiles
+  static constexpr int T_SFW = 2 * MAXTOK;
   static constexpr int T_SFX = T_SFW + 4 * STAGES;
   static constexpr int T_END = T_SFX + 4 * STAGES;
-  static constexpr int TMEM_COLS = T_END <= 32 ? 32 : (T_END <= 64 ? 64 : 128);
-  static_assert(T_END <= 128, "tensor memory");
+  static constexpr int TMEM_COLS = T_END <= 32 ? 32 : (T_END <= 64 ? 64 : (T_END <= 128 ? 128 : 256));
+  static_assert(T_END <= 256, "tensor memory");
   static_assert(MINB * SMEM_ALLOC <= 232448, "shared memory");
   static_assert(QTHREADS % kRows == 0, "each reduction thread owns one output column");
 };
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       mbar_init(&full_x[s], QTHREADS / 32);  // one arrive per quantiser warp
       mbar_init(&x_empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);  // one commit per MMA issuer
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmW);
@@ -185,12 +190,15 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMma2Warp) {
+    // ------------------------------------------------ MMA issuers: even K tiles
+    // into one accumulator, odd into another (summed in fixed order below)
     if (lane == 0) {
+      const int par = warp == 1 ? 0 : 1;
+      const uint32_t t_acc = tmem + (par ? C::T_ACC1 : C::T_ACC);
       const uint32_t idesc0 = idesc_mxf8(kRows, a.n_mma);
       bool ok = true;
-      for (int i = 0; i < nk && ok; ++i) {
+      for (int i = par; i < nk && ok; i += 2) {
         const int st = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
         const int xs = i % C::XSTAGES;
@@ -210,8 +218,8 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(smem + C::OFF_X + xs * C::XBYTES));
 #pragma unroll
         for (int kk = 0; kk < kTK / 32; ++kk)
-          tc_mma_mxf8(tmem + C::T_ACC, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk), t_sfw,
-                      t_sfx, (i | kk) != 0);
+          tc_mma_mxf8(t_acc, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk), t_sfw, t_sfx,
+                      i >= 2 || kk != 0);
         tc_commit(&empty[st]);
         tc_commit(&x_empty[xs]);
       }
@@ -219,8 +227,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       else __nanosleep(200000);  // let issued tensor-core work retire
     }
     __syncwarp();
-  } else {
-    // x is written by the previous kernel in the stream: wait for it to finish.
+  } else if (warp < kMma2Warp) {
     // Token rows M .. n_mma - 1 are zero in every K tile: write their codes and
     // scale bytes once, before the dependency wait, and quantise only rows < M
     // afterwards (a zero block quantises to byte 0 and zero codes, so this is
@@ -238,6 +245,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
           *reinterpret_cast<uint32_t*>(smem + C::OFF_SFX + xs * kAtomBytes + (row & 31) * 16 + (row >> 5) * 4) = 0u;
       }
     }
+    // x is written by the previous kernel in the stream: wait for it to finish.
     grid_dependency_wait();
     // ------------------------------------------------ activation quantiser
     // A task is one 32-element block of x: K tile i, token row r < M, block j
@@ -316,11 +324,16 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       const uint32_t dst = map_shared_rank(smem_u32(smem + C::OFF_RECV), owner) +
                            static_cast<uint32_t>(((rank * a.n_mma) * per + nl) * 4);
       for (int c = 0; c < a.n_mma; c += 16) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + c, r);
+        uint32_t r[16], r1[16];
+        const uint32_t lrow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        tmem_ld_32x32b_x16(lrow + C::T_ACC + c, r);
+        tmem_ld_32x32b_x16(lrow + C::T_ACC1 + c, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) st_shared_cluster_u32(dst + static_cast<uint32_t>((c + j) * per * 4), r[j]);
+        for (int j = 0; j < 16; ++j) {
+          const float v = nk > 1 ? __uint_as_float(r[j]) + __uint_as_float(r1[j]) : __uint_as_float(r[j]);
+          st_shared_cluster_u32(dst + static_cast<uint32_t>((c + j) * per * 4), __float_as_uint(v));
+        }
       }
     }
   }
@@ -328,7 +341,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
   // ------------------------------------------------ split-K reduction (owner sums)
   tc_fence_before();
   cluster_sync();  // all partials have landed in their owners' receive buffers
-  if (threadIdx.x >= 64 && !*abort_flag) {
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + QTHREADS && !*abort_flag) {
     const int t = threadIdx.x - 64;
     const int per = kRows / a.splits;
     const float* recv = reinterpret_cast<const float*>(smem + C::OFF_RECV);
