@@ -30,7 +30,9 @@
 //                K tiles ahead, and once a pair of stages is free tcgen05.st
 //                them (all 256 weight columns, in order: each CTA's half of
 //                the pair MMA reads the scales from its own tensor memory),
-//                then arrive on the even CTA's sf_ready barrier of the pair;
+//                then arrive on the even CTA's sf_ready barrier of the pair
+//                (the even CTA's writers first wait for both stages' operands,
+//                so the MMA issuer waits once per two stages);
 //   warps 6..13  epilogue: drain this CTA's accumulator as bf16, arrive on the
 //                even CTA's acc_empty barrier, TMA-store the rows.
 // One thread issuing every copy of a stage is the first limit here (a TMA or
@@ -239,8 +241,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         tc_fence_after();
         for (int kt = 0; kt < args.KT; ++kt) {
           // operands of both CTAs landed, and both CTAs' scales are in TMEM
-          if (!mbar_wait(&full[stage], phase, abort_flag) ||
-              !mbar_wait(&sf_ready[stage >> 1], phase, abort_flag)) {
+          // one wait per pair of stages: the even CTA's scale writers arrive on
+          // sf_ready only after both stages' operands have landed
+          if ((stage & 1) == 0 && !mbar_wait(&sf_ready[stage >> 1], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -349,9 +352,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader)
-            mbar_arrive(&sf_ready[stage >> 1]);
-          else
+          if (leader) {
+            // the operands of both stages (both CTAs' copies complete here)
+            bool landed = mbar_wait(&full[stage], phase, abort_flag);
+            if (landed && two) landed = mbar_wait(&full[stage + 1], phase, abort_flag);
+            if (landed) mbar_arrive(&sf_ready[stage >> 1]);
+          } else
             mbar_arrive_remote(ready_even + static_cast<uint32_t>((stage >> 1) * 8));
         }
         stage += 2;
