@@ -11,14 +11,16 @@
 //     on padding tokens;
 //   * K is split over a cluster of S CTAs (S in {1, 2, 4, 8}, the largest
 //     whose clusters all fit on the GPU at once); each CTA streams its
-//     128 x K/S weight slice through a TMA ring (at N = K = 4096 and M <= 16:
-//     S = 8, 4 K tiles per CTA, the whole slice in flight from the start);
+//     128 x K/S weight slice through a TMA ring (at N = K = 4096: S = 4 -- at
+//     one CTA per SM only 15 clusters of 8 fit at once -- so 8 K tiles per
+//     CTA, which up to 16 tokens are all in flight from the start);
 //   * warps 2..9 read x (bf16, from L2) and quantise it with the same device
-//     function as the standalone quantize kernel, writing E4M3 codes straight
-//     into the 128-byte-swizzled operand tile and the scales into the
-//     scale-factor atom.  They work on groups of K tiles and issue the next
-//     group's loads before quantising the current one, so the latency of x is
-//     paid about once;
+//     function as the standalone quantize kernel (one lane per 32-element
+//     block of the M real token rows), writing E4M3 codes straight into the
+//     128-byte-swizzled operand tile and the scales into the scale-factor
+//     atom.  They work on groups of K tiles and issue the next group's loads
+//     before quantising the current one, so the latency of x is paid about
+//     once;
 //   * the S fp32 partial tiles meet in distributed shared memory: CTA r owns
 //     weight rows [r*128/S, (r+1)*128/S); every CTA stores its partial for
 //     those rows straight into the owner's receive buffer (remote shared-memory
@@ -32,7 +34,7 @@
 //     shared slots, quantising the second half of a CTA's K slice had to wait
 //     for the MMAs of the first half, a round trip on every call's critical
 //     path (dependency wait -> x -> MMAs -> reduction).
-// Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~160 KB of
+// Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~165 KB of
 // shared memory) and up to 64 tokens (6-stage weight ring), one CTA per SM.
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
 // and MMA issuer for the even K tiles, 10 = MMA issuer for the odd K tiles
