@@ -242,10 +242,12 @@ def _bf16_exact_block_input(M, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (4, 256, 512), (16, 136, 1024), (33, 264, 256),
-                                   (64, 128, 4096)])
+                                   (64, 128, 4096), (5, 256, 1536), (40, 136, 3072)])
 def test_small_m_path_exact_block_scales(M, N, K):
     """x with a distinct power-of-two block scale per (row, block), integer W:
-    exact sums, so the small-M path must equal bf16(oracle) bit for bit."""
+    exact sums, so the small-M path must equal bf16(oracle) bit for bit.
+    K = 1536 and 3072 give each CTA of the K split an odd number (3) of K
+    tiles, which the two MMA issuers divide unevenly."""
     dev = device()
     x = _bf16_exact_block_input(M, K, seed=M + K)
     rng = np.random.default_rng(N)
