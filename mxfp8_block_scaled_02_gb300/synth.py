@@ -90,9 +90,10 @@ def to_bf16_bits(v: np.ndarray) -> np.ndarray:
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
-    """Exact widening of bf16 bit patterns to fp64."""
+    """Exact widening of bf16 bit patterns to fp64 (NaN patterns stay NaN)."""
     b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns raise the flag on widening
+        return b.view(np.float32).astype(np.float64)
 
 
 @dataclasses.dataclass
