@@ -100,3 +100,10 @@ def test_python_binding_validates_shapes():
 def test_build_entry_point_is_importable():
     import __graft_entry__ as g
     assert callable(g.build) and callable(g.smoke)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    # no fallback path: without the built library every call raises
+    monkeypatch.setattr(ops, "_lib", None)
+    with pytest.raises(RuntimeError, match="is missing"):
+        ops.load(str(tmp_path / "libmxfp8.so"))
