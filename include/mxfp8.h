@@ -73,8 +73,9 @@ int mxfp8_version(void);
  *   scale byte 0; a block holding Inf or NaN gets 0xFF and elements 0x7F.
  *   x_bf16  : device, [rows, K] bf16, 16-byte aligned.
  *   x_q     : device, [rows, K] E4M3 codes out, 16-byte aligned.
- *   x_scale : device, [rows, K/32] E8M0 bytes out (row-major).
- *   rows >= 0 (0 is a no-op), K > 0 and K % 32 == 0.
+ *   x_scale : device, [rows, K/32] E8M0 bytes out (row-major), 16-byte aligned.
+ *   rows >= 0 (0 is a no-op), K > 0 and K % 32 == 0; rows * K/32 above
+ *   2^31 - 1 blocks returns MXFP8_ERR_UNSUPPORTED (split the call).
  */
 mxfp8_status mxfp8_quantize(const void* x_bf16, int64_t rows, int64_t K, uint8_t* x_q,
                             uint8_t* x_scale, mxfp8_stream_t stream);
@@ -94,12 +95,16 @@ mxfp8_status mxfp8_packed_sizes(int64_t B, int64_t N, int64_t K, size_t* w_bytes
  *   page) and "CompressedTensorsW8A8Mxfp8.create_weights" (weight [N, K] E4M3,
  *   weight_scale [N, K/32] uint8).
  *   w        : device, [B, N, K] E4M3 codes (row-major, K contiguous).
- *   w_scale  : device, [B, N, K/32] E8M0 bytes (row-major).
+ *   w_scale  : device, [B, N, K/32] E8M0 bytes (row-major), exactly K/32
+ *              per row (a checkpoint whose scales are padded is sliced to
+ *              [:N, :K/32] and made contiguous by the caller first).
  *   w_packed : device, w_bytes out: the E4M3 codes, K-major as the tensor cores
  *              read them (the same bytes as w; w_packed == w is allowed).
  *   sf_packed: device, sf_bytes out: the scales in 512-byte atoms of 128 rows x
  *              4 blocks, the tensor cores' scale-factor layout; padding is zero.
- *   B >= 1, N > 0, K > 0, K % 32 == 0.  Pointers 16-byte aligned.
+ *   B >= 1, N > 0, K > 0, K % 32 == 0.  Every pointer 16-byte aligned
+ *   (MXFP8_ERR_INVALID_ARG otherwise, before any launch).  More than 2^31 - 1
+ *   scale blocks returns MXFP8_ERR_UNSUPPORTED.
  */
 mxfp8_status mxfp8_process_weights(const uint8_t* w, const uint8_t* w_scale, int64_t B,
                                    int64_t N, int64_t K, uint8_t* w_packed,
@@ -140,13 +145,22 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
  *   The accumulation is fp32 on the tensor cores and the result is rounded once
  *   to bf16 after the bias add.  Requirements: B >= 1, M >= 0 (0 is a no-op),
  *   N > 0 with N % 8 == 0, K > 0 with K % 128 == 0 (else MXFP8_ERR_UNSUPPORTED),
- *   all pointers 16-byte aligned.
+ *   all pointers (x_scale included) 16-byte aligned (else
+ *   MXFP8_ERR_INVALID_ARG), at most 2^31 - 1 scale blocks in x and in w.
  *   Stream ordering: the GEMM kernels are launched with programmatic stream
  *   serialization.  When the kernel before them in the stream triggers its
  *   dependents early (griddepcontrol.launch_dependents), they may read
  *   w_packed, sf_packed and bias before that kernel ends; x, x_q, x_scale
- *   and out are touched only after it has finished.  Kernels launched the
- *   ordinary way never trigger early, so for them this is plain stream order.
+ *   and out are touched only after it has finished.  Of this library's
+ *   kernels, only these trigger early: the quantise / activation-scale repack
+ *   step inside mxfp8_linear, mxfp8_linear_path and mxfp8_linear_noalloc
+ *   (whose output only the same call's GEMM reads, after its wait), and the
+ *   small-M GEMM (whose output the next layer reads as x, after its wait).
+ *   The standalone calls (mxfp8_quantize, mxfp8_quantize_packed,
+ *   mxfp8_pack_scales, mxfp8_process_weights) never do, so weights they write
+ *   are complete before a GEMM queued after them starts.  Kernels from other
+ *   code trigger early only if they say so; for them this is plain stream
+ *   order.
  */
 mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,
                           int64_t B, int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
@@ -185,7 +199,8 @@ mxfp8_status mxfp8_quantize_packed(const void* x_bf16, int64_t B, int64_t M, int
 /*
  * mxfp8_pack_scales - row-major E8M0 scales [B, R, K/32] -> packed atoms
  * (zero padding), for any operand; mxfp8_process_weights uses it for weight
- * scales and mxfp8_linear for pre-quantised activation scales.
+ * scales and mxfp8_linear for pre-quantised activation scales.  scale and
+ * sf_packed: device, 16-byte aligned.
  */
 mxfp8_status mxfp8_pack_scales(const uint8_t* scale, int64_t B, int64_t R, int64_t K,
                                uint8_t* sf_packed, mxfp8_stream_t stream);

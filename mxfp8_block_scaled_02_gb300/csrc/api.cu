@@ -37,6 +37,8 @@ mxfp8_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MXFP8_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
 struct DeviceInfo {
   bool ok = false;
   int sms = 0;
@@ -69,8 +71,6 @@ mxfp8_status current_device(int* sms) {
   return MXFP8_OK;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kSmallM = mx::kDecodeMaxM;  // largest M the fused small-M path serves
@@ -89,11 +89,26 @@ WsLayout prefill_workspace(int64_t B, int64_t M, int64_t K, bool quantized) {
   return w;
 }
 
+// The quantise and repack kernels index 32-element blocks and 4-byte packed
+// scale words with 32-bit integers: B*R*(K/32) blocks and the packed scale
+// words of (B, R, K) must each fit in 31 bits.  Sizes are checked for range
+// first, so the products below cannot overflow 64 bits.
+mxfp8_status check_block_count(int64_t B, int64_t R, int64_t K, const char* what) {
+  if (B > (1ll << 20) || R > (1ll << 31) || K > (1ll << 30) || B * R > (1ll << 31) ||
+      B * R * (K / 32) > mx::kMaxBlocks32 || mx::sf_packed_bytes(B, R, K) / 4 > mx::kMaxBlocks32)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "%s: B=%lld R=%lld K=%lld has more than 2^31 - 1 scale blocks; split the call",
+                what, (long long)B, (long long)R, (long long)K);
+  return MXFP8_OK;
+}
+
 mxfp8_status check_weights_args(const void* w, const void* ws, int64_t B, int64_t N, int64_t K) {
   if (w == nullptr || ws == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null weight pointer");
   if (B < 1 || N < 1 || K < 1) return fail(MXFP8_ERR_INVALID_ARG, "B=%lld N=%lld K=%lld", (long long)B, (long long)N, (long long)K);
   if (K % 32 != 0) return fail(MXFP8_ERR_INVALID_ARG, "K=%lld is not a multiple of 32", (long long)K);
-  return MXFP8_OK;
+  if (!aligned(w, 16) || !aligned(ws, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "weight and scale pointers must be 16-byte aligned");
+  return check_block_count(B, N, K, "scales");
 }
 
 mxfp8_status check_gemm_args(int64_t B, int64_t M, int64_t N, int64_t K) {
@@ -107,7 +122,11 @@ mxfp8_status check_gemm_args(int64_t B, int64_t M, int64_t N, int64_t K) {
     return fail(MXFP8_ERR_UNSUPPORTED, "N=%lld: this library needs N %% 8 == 0", (long long)N);
   if (B * M > (1ll << 31) || N > (1ll << 30) || K > (1ll << 30))
     return fail(MXFP8_ERR_UNSUPPORTED, "problem too large");
-  return MXFP8_OK;
+  if (M > 0) {
+    mxfp8_status st = check_block_count(B, M, K, "activations");
+    if (st != MXFP8_OK) return st;
+  }
+  return check_block_count(B, N, K, "weights");
 }
 
 }  // namespace
@@ -144,13 +163,14 @@ mxfp8_status mxfp8_quantize(const void* x_bf16, int64_t rows, int64_t K, uint8_t
   if (rows == 0) return MXFP8_OK;
   if (x_bf16 == nullptr || x_q == nullptr || x_scale == nullptr)
     return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
-  if (!aligned(x_bf16, 16) || !aligned(x_q, 16))
-    return fail(MXFP8_ERR_INVALID_ARG, "x_bf16 and x_q must be 16-byte aligned");
-  int sms = 0;
-  mxfp8_status st = current_device(&sms);
+  if (!aligned(x_bf16, 16) || !aligned(x_q, 16) || !aligned(x_scale, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "x_bf16, x_q and x_scale must be 16-byte aligned");
+  mxfp8_status st = check_block_count(1, rows, K, "mxfp8_quantize");
   if (st != MXFP8_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
   cudaError_t e = mx::launch_quantize(x_bf16, rows, K, x_q, x_scale, false, 1, rows, sms,
-                                      reinterpret_cast<cudaStream_t>(stream));
+                                      reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return MXFP8_OK;
 }
@@ -170,8 +190,8 @@ mxfp8_status mxfp8_process_weights(const uint8_t* w, const uint8_t* w_scale, int
   mxfp8_status st = check_weights_args(w, w_scale, B, N, K);
   if (st != MXFP8_OK) return st;
   if (w_packed == nullptr || sf_packed == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
-  if (!aligned(w, 16) || !aligned(w_packed, 16) || !aligned(sf_packed, 16))
-    return fail(MXFP8_ERR_INVALID_ARG, "w, w_packed and sf_packed must be 16-byte aligned");
+  if (!aligned(w_packed, 16) || !aligned(sf_packed, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "w_packed and sf_packed must be 16-byte aligned");
   int sms = 0;
   if ((st = current_device(&sms)) != MXFP8_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -179,7 +199,7 @@ mxfp8_status mxfp8_process_weights(const uint8_t* w, const uint8_t* w_scale, int
     cudaError_t e = cudaMemcpyAsync(w_packed, w, static_cast<size_t>(B * N * K), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "weight copy");
   }
-  cudaError_t e = mx::launch_sf_pack(w_scale, B, N, K, sf_packed, sms, s);
+  cudaError_t e = mx::launch_sf_pack(w_scale, B, N, K, sf_packed, sms, s, false);
   if (e != cudaSuccess) return cuda_fail(e, "scale repack launch");
   return MXFP8_OK;
 }
@@ -226,10 +246,9 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
   if (w_packed == nullptr || sf_packed == nullptr || out_bf16 == nullptr)
     return fail(MXFP8_ERR_INVALID_ARG, "null weight or output pointer");
   if (!aligned(w_packed, 16) || !aligned(sf_packed, 16) || !aligned(out_bf16, 16) ||
-      (have_x && !aligned(x_bf16, 16)) || (have_q && !aligned(x_q, 16)) ||
+      (have_x && !aligned(x_bf16, 16)) || (have_q && (!aligned(x_q, 16) || !aligned(x_scale, 16))) ||
       (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
     return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (M == 0) return MXFP8_OK;
   int sms = 0;
   mxfp8_status st = current_device(&sms);
   if (st != MXFP8_OK) return st;
@@ -258,11 +277,11 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
   cudaError_t e;
   if (have_x) {
     uint8_t* xq = wsb + ws.xq_off;
-    e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s);
+    e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     a = xq;
   } else {
-    e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s);
+    e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
   mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0)};
@@ -289,23 +308,24 @@ mxfp8_status mxfp8_quantize_packed(const void* x_bf16, int64_t B, int64_t M, int
     return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
   if (!aligned(x_bf16, 16) || !aligned(x_q, 16) || !aligned(sfa_packed, 16))
     return fail(MXFP8_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  int sms = 0;
-  mxfp8_status st = current_device(&sms);
+  mxfp8_status st = check_block_count(B, M, K, "mxfp8_quantize_packed");
   if (st != MXFP8_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
   cudaError_t e = mx::launch_quantize(x_bf16, B * M, K, x_q, sfa_packed, true, B, M, sms,
-                                      reinterpret_cast<cudaStream_t>(stream));
+                                      reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return MXFP8_OK;
 }
 
 mxfp8_status mxfp8_pack_scales(const uint8_t* scale, int64_t B, int64_t R, int64_t K,
                                uint8_t* sf_packed, mxfp8_stream_t stream) {
-  mxfp8_status st = check_weights_args(scale, sf_packed, B, R, K);
+  mxfp8_status st = check_weights_args(scale, sf_packed, B, R, K);  // both pointers 16-byte aligned
   if (st != MXFP8_OK) return st;
-  if (!aligned(sf_packed, 16)) return fail(MXFP8_ERR_INVALID_ARG, "sf_packed must be 16-byte aligned");
   int sms = 0;
   if ((st = current_device(&sms)) != MXFP8_OK) return st;
-  cudaError_t e = mx::launch_sf_pack(scale, B, R, K, sf_packed, sms, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = mx::launch_sf_pack(scale, B, R, K, sf_packed, sms, reinterpret_cast<cudaStream_t>(stream),
+                                     false);
   if (e != cudaSuccess) return cuda_fail(e, "scale repack launch");
   return MXFP8_OK;
 }

@@ -8,12 +8,19 @@
 
 namespace mx {
 
-// quantize.cu
+// quantize.cu.  The kernels index 32-element blocks and 4-byte scale words
+// with 32-bit integers: the host refuses larger problems before launching.
+constexpr int64_t kMaxBlocks32 = 0x7FFFFFFFll;
+// early_trigger: let the next kernel in the stream start before this one ends
+// (programmatic dependent launch).  Only for the activation quantise / scale
+// repack inside the linear layer: the GEMM that follows reads their output
+// after its dependency wait.  Never for weights (the GEMMs load weights and
+// weight scales before that wait).
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
                             bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool early_trigger);
 cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
-                           int sms, cudaStream_t stream);
+                           int sms, cudaStream_t stream, bool early_trigger);
 cudaError_t launch_sf_unpack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
                              int sms, cudaStream_t stream);
 cudaError_t take_status_quantize(unsigned int* out);

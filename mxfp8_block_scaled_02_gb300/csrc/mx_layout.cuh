@@ -12,7 +12,9 @@
 //                                                  KT = ceil(K / 128)
 // so the atoms of consecutive 128-row tiles at one K tile are adjacent, and a
 // 256-row operand tile reads 1 KB contiguous per K tile.  Rows >= R and blocks
-// >= K/32 are padding and hold 0.
+// >= K/32 are padding.  The scale repack (sf_pack_kernel) writes them as 0;
+// the quantise kernel writing packed scales leaves them as they were, which
+// only affects accumulator rows >= R, and those are never stored.
 #pragma once
 
 #include <stdint.h>

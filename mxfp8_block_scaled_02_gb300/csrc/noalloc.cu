@@ -104,7 +104,7 @@ extern "C" mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int6
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* xq = scratch;
   uint8_t* sfa = scratch + xq_bytes;
-  cudaError_t e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s);
+  cudaError_t e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s, true);
   if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "mxfp8_linear_noalloc: quantize launch failed");
   mx::GemmProblem p{xq, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K};
   const char* msg = "";

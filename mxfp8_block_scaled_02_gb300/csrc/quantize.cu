@@ -25,14 +25,15 @@ constexpr int kQU = 2;  // 32-block warp tasks per loop iteration, loads all in 
 // scale is byte g of s.  Lane l of a warp task takes block 32 t + l, so a warp
 // reads 2 KB and writes 1 KB of codes and 32 scale bytes, contiguous.
 // kPacked selects the 512-byte atom layout of mx_layout.cuh for the scales
-// (rows grouped per batch of rows_per_b).
-template <bool kPacked>
+// (rows grouped per batch of rows_per_b).  kEarly lets the next kernel in the
+// stream start at once (griddepcontrol.launch_dependents): only for the
+// quantise step inside the linear layer, whose GEMM reads the codes and scales
+// after its own dependency wait and loads nothing this kernel writes before it.
+template <bool kPacked, bool kEarly>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     const uint4* __restrict__ x, uint32_t total_blocks, uint32_t KB, uint8_t* __restrict__ q,
     uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT, uint32_t KT) {
-  // The GEMM that follows may start its prologue and weight loads now; it
-  // waits for this grid to finish before it reads the codes and scales.
-  launch_dependents();
+  if (kEarly) launch_dependents();
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -79,12 +80,16 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
 
 // Row-major [B, R, KB] -> packed atoms; one thread per 4 output bytes (the 4
 // blocks of one row inside an atom).  Padding rows/blocks are written as 0.
-// 32-bit index arithmetic (the launcher checks the sizes): 64-bit divisions
-// per word made this repack cost ~20 us for 3.7 MB of scales.
+// 32-bit index arithmetic (the host checks the sizes): 64-bit divisions per
+// word made this repack cost ~20 us for 3.7 MB of scales.  kEarly as for the
+// quantise kernel: only the activation-scale repack inside the linear layer
+// triggers its dependents early; a weight repack never does, because the GEMMs
+// load weight scales before their dependency wait.
+template <bool kEarly>
 __global__ void __launch_bounds__(256) sf_pack_kernel(const uint8_t* __restrict__ src, uint32_t R,
                                                        uint32_t KB, uint32_t RT, uint32_t KT,
                                                        uint32_t* __restrict__ dst, uint32_t nwords) {
-  launch_dependents();  // the GEMM that follows waits for this grid before it reads the atoms
+  if (kEarly) launch_dependents();
   const uint32_t stride = gridDim.x * blockDim.x;
   for (uint32_t wi = blockIdx.x * blockDim.x + threadIdx.x; wi < nwords; wi += stride) {
     const uint32_t atom = wi >> 7;  // 128 words per 512-byte atom
@@ -138,46 +143,50 @@ int grid_for(int64_t work_items, int threads, int sms, int per_sm) {
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
-                            bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
-                            cudaStream_t stream) {
-  (void)B;
-  const int64_t KB = K / 32;
-  const int64_t total_blocks = rows * KB;
-  if (total_blocks == 0) return cudaSuccess;
-  if (total_blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-  static int per_sm[2] = {0, 0};
-  int& occ = per_sm[packed_scales ? 1 : 0];
-  if (occ == 0) {
-    cudaError_t e = packed_scales
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<true>, kQuantThreads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, quantize_kernel<false>, kQuantThreads, 0);
-    if (e != cudaSuccess || occ < 1) occ = 1;
+template <bool kPacked, bool kEarly>
+cudaError_t launch_quantize_t(const void* x, int64_t total_blocks, int64_t K, uint8_t* q, uint8_t* s,
+                              int64_t rows_per_b, int sms, cudaStream_t stream) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<kPacked, kEarly>,
+                                                                  kQuantThreads, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
   }
   const int64_t ntasks = ceil_div(total_blocks, 32);
-  const int grid = grid_for(ceil_div(ntasks, kQU) * 32, kQuantThreads, sms, occ);
+  const int grid = grid_for(ceil_div(ntasks, kQU) * 32, kQuantThreads, sms, per_sm);
   const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
   const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
-  if (packed_scales)
-    quantize_kernel<true><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(KB), q, s,
-        static_cast<uint32_t>(rows_per_b), RT, KT);
-  else
-    quantize_kernel<false><<<grid, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(KB), q, s,
-        static_cast<uint32_t>(rows_per_b), RT, KT);
+  quantize_kernel<kPacked, kEarly><<<grid, kQuantThreads, 0, stream>>>(
+      static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(K / 32), q, s,
+      static_cast<uint32_t>(rows_per_b), RT, KT);
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                            bool packed_scales, int64_t B, int64_t rows_per_b, int sms,
+                            cudaStream_t stream, bool early_trigger) {
+  (void)B;
+  const int64_t total_blocks = rows * (K / 32);
+  if (total_blocks == 0) return cudaSuccess;
+  if (total_blocks > kMaxBlocks32) return cudaErrorInvalidValue;  // the host refuses these first
+  if (packed_scales)
+    return early_trigger ? launch_quantize_t<true, true>(x, total_blocks, K, q, s, rows_per_b, sms, stream)
+                         : launch_quantize_t<true, false>(x, total_blocks, K, q, s, rows_per_b, sms, stream);
+  return early_trigger ? launch_quantize_t<false, true>(x, total_blocks, K, q, s, rows_per_b, sms, stream)
+                       : launch_quantize_t<false, false>(x, total_blocks, K, q, s, rows_per_b, sms, stream);
+}
+
 cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
-                           int sms, cudaStream_t stream) {
+                           int sms, cudaStream_t stream, bool early_trigger) {
   const int64_t KB = K / 32, RT = ceil_div(R, kAtomRows), KT = ceil_div(K, kTileK);
   const int64_t nwords = sf_packed_bytes(B, R, K) / 4;
   if (nwords == 0) return cudaSuccess;
-  if (nwords > 0x7FFFFFFFll || B * R * KB > 0x7FFFFFFFll) return cudaErrorInvalidValue;
-  sf_pack_kernel<<<grid_for(nwords, 256, sms, 8), 256, 0, stream>>>(
-      src, static_cast<uint32_t>(R), static_cast<uint32_t>(KB), static_cast<uint32_t>(RT),
-      static_cast<uint32_t>(KT), reinterpret_cast<uint32_t*>(dst), static_cast<uint32_t>(nwords));
+  if (nwords > kMaxBlocks32 || B * R * KB > kMaxBlocks32) return cudaErrorInvalidValue;  // refused by the host first
+  const int grid = grid_for(nwords, 256, sms, 8);
+  auto kern = early_trigger ? sf_pack_kernel<true> : sf_pack_kernel<false>;
+  kern<<<grid, 256, 0, stream>>>(src, static_cast<uint32_t>(R), static_cast<uint32_t>(KB),
+                                 static_cast<uint32_t>(RT), static_cast<uint32_t>(KT),
+                                 reinterpret_cast<uint32_t*>(dst), static_cast<uint32_t>(nwords));
   return cudaGetLastError();
 }
 

@@ -101,11 +101,20 @@ def _require_cuda(*ts: torch.Tensor | None) -> None:
                 raise ValueError("tensors must be contiguous")
 
 
+def _aligned16(t: torch.Tensor | None) -> torch.Tensor | None:
+    """The same values at a 16-byte aligned address (every pointer the ABI takes
+    must be; a view into a larger tensor may not be), copied only if needed."""
+    if t is None or t.data_ptr() % 16 == 0:
+        return t
+    return t.clone(memory_format=torch.contiguous_format)
+
+
 def quantize(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
     """bf16 x [..., K] -> (x_q uint8 E4M3 [..., K], x_scale uint8 E8M0 [..., K/32])."""
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
     _require_cuda(x)
+    x = _aligned16(x)
     K = x.shape[-1]
     rows = x.numel() // K if K else 0
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
@@ -133,15 +142,28 @@ class PackedWeights:
 
 
 def process_weights(w_q: torch.Tensor, w_scale: torch.Tensor) -> PackedWeights:
-    """w_q [N, K] or [B, N, K] (uint8 or float8_e4m3fn), w_scale [..., K/32] uint8."""
-    _require_cuda(w_q, w_scale)
-    batched = w_q.dim() == 3
+    """w_q [N, K] or [B, N, K] (uint8 or float8_e4m3fn), w_scale [..., K/32] uint8.
+
+    A checkpoint may store its scales padded (more rows than N or more blocks
+    than K/32, as the aiter_flydsl page's process_weights_after_loading slices
+    them with ``[:N, :K // 32]``): the padding is sliced off here and the
+    scales copied to a dense, aligned tensor before the repack.
+    """
     if w_q.dim() not in (2, 3):
         raise ValueError("w_q must be [N, K] or [B, N, K]")
+    batched = w_q.dim() == 3
     B = w_q.shape[0] if batched else 1
     N, K = w_q.shape[-2], w_q.shape[-1]
-    if tuple(w_scale.shape) != (*w_q.shape[:-1], K // BLOCK):
+    if K % BLOCK:
+        raise ValueError(f"K={K} is not a multiple of {BLOCK}")
+    if (w_scale.dim() != w_q.dim() or tuple(w_scale.shape[:-2]) != tuple(w_q.shape[:-2])
+            or w_scale.shape[-2] < N or w_scale.shape[-1] < K // BLOCK):
         raise ValueError(f"weight scale {tuple(w_scale.shape)} does not match weight {tuple(w_q.shape)}")
+    w_scale = w_scale[..., :N, :K // BLOCK]
+    if not w_scale.is_contiguous():
+        w_scale = w_scale.contiguous()
+    w_q, w_scale = _aligned16(w_q), _aligned16(w_scale)
+    _require_cuda(w_q, w_scale)
     wb, sb = packed_sizes(B, N, K)
     wp = torch.empty(wb, dtype=torch.uint8, device=w_q.device)
     sp = torch.empty(sb, dtype=torch.uint8, device=w_q.device)
@@ -162,6 +184,38 @@ def workspace_size(B: int, M: int, N: int, K: int, quantized: bool) -> int:
     return n.value
 
 
+def _linear_rows(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None,
+                 x_scale: torch.Tensor | None, out: torch.Tensor | None) -> int:
+    """Check x (and x_scale, bias, out) against the packed weights; returns M,
+    the rows per batch.  Shared by every linear entry point, so that none of
+    them hands the library a buffer shorter than the sizes it is told."""
+    quantized = x_scale is not None
+    if not quantized and x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16 (or pass x_scale with a pre-quantised x)")
+    if quantized and x.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("a pre-quantised x must be uint8 or float8_e4m3fn E4M3 codes")
+    _require_cuda(x, x_scale, bias, out)
+    if x.dim() < 1:
+        raise ValueError("x must have a K dimension")
+    K = x.shape[-1]
+    if K != pw.K:
+        raise ValueError(f"x has K={K}, weights have K={pw.K}")
+    if pw.batched:
+        if x.dim() != 3 or x.shape[0] != pw.B:
+            raise ValueError("batched weights need x of shape [B, M, K]")
+        M = x.shape[1]
+    else:
+        M = x.numel() // K if K else 0
+    if quantized and (x_scale.dtype not in (torch.uint8, torch.float8_e8m0fnu)
+                      or tuple(x_scale.shape) != (*x.shape[:-1], K // BLOCK)):
+        raise ValueError(f"MXFP8 activation scale {tuple(x_scale.shape)} for {tuple(x.shape)}")
+    if bias is not None and (bias.dtype != torch.bfloat16 or tuple(bias.shape) != (pw.N,)):
+        raise ValueError("bias must be bf16 [N]")
+    if out is not None and (out.dtype != torch.bfloat16 or out.numel() != pw.B * M * pw.N):
+        raise ValueError(f"out must be bf16 with {pw.B * M * pw.N} elements")
+    return M
+
+
 def linear(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
            x_scale: torch.Tensor | None = None, *, path: int = 0,
            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
@@ -175,22 +229,9 @@ def linear(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
     choose.
     """
     quantized = x_scale is not None
-    if not quantized and x.dtype != torch.bfloat16:
-        raise TypeError("x must be bfloat16 (or pass x_scale with a pre-quantised x)")
-    _require_cuda(x, x_scale, bias)
-    K = x.shape[-1]
-    if K != pw.K:
-        raise ValueError(f"x has K={K}, weights have K={pw.K}")
-    if pw.batched:
-        if x.dim() != 3 or x.shape[0] != pw.B:
-            raise ValueError("batched weights need x of shape [B, M, K]")
-        M = x.shape[1]
-    else:
-        M = x.numel() // K if K else 0
-    if quantized and tuple(x_scale.shape) != (*x.shape[:-1], K // BLOCK):
-        raise ValueError(f"MXFP8 activation scale {tuple(x_scale.shape)} for {tuple(x.shape)}")
-    if bias is not None and (bias.dtype != torch.bfloat16 or tuple(bias.shape) != (pw.N,)):
-        raise ValueError("bias must be bf16 [N]")
+    M = _linear_rows(x, pw, bias, x_scale, out)
+    K = pw.K
+    x, x_scale, bias = _aligned16(x), _aligned16(x_scale), _aligned16(bias)
     if out is None:
         out = torch.empty((*x.shape[:-1], pw.N), dtype=torch.bfloat16, device=x.device)
     if M == 0:
@@ -223,6 +264,7 @@ def quantize_packed(x: torch.Tensor, B: int = 1, *, x_q: torch.Tensor | None = N
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
     _require_cuda(x)
+    x = _aligned16(x)
     K = x.shape[-1]
     M = x.numel() // (K * B)
     if x_q is None:
@@ -236,6 +278,7 @@ def quantize_packed(x: torch.Tensor, B: int = 1, *, x_q: torch.Tensor | None = N
 def pack_scales(scale: torch.Tensor, B: int = 1) -> torch.Tensor:
     """Row-major E8M0 scales [B, R, K/32] (or [R, K/32]) -> packed atoms."""
     _require_cuda(scale)
+    scale = _aligned16(scale)
     KB = scale.shape[-1]
     R = scale.numel() // (KB * B)
     out = torch.empty(packed_sizes(B, R, KB * BLOCK)[1], dtype=torch.uint8, device=scale.device)
@@ -267,15 +310,13 @@ def linear_noalloc(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None
     the GPU share that array and race.  Only ``out`` is allocated here when it
     is not given.
     """
-    if x.dtype != torch.bfloat16:
-        raise TypeError("x must be bfloat16")
-    _require_cuda(x, bias, out)
-    K = x.shape[-1]
-    if K != pw.K:
-        raise ValueError(f"x has K={K}, weights have K={pw.K}")
-    M = x.shape[1] if pw.batched else (x.numel() // K if K else 0)
+    M = _linear_rows(x, pw, bias, None, out)
+    K = pw.K
+    x, bias = _aligned16(x), _aligned16(bias)
     if out is None:
         out = torch.empty((*x.shape[:-1], pw.N), dtype=torch.bfloat16, device=x.device)
+    if M == 0:
+        return out
     _check(load().mxfp8_linear_noalloc(_ptr(x), pw.B, M, pw.N, K, _ptr(pw.w_packed),
                                        _ptr(pw.sf_packed), _ptr(bias), _ptr(out), _stream()))
     return out

@@ -90,6 +90,54 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert lib.mxfp8_debug_expire_wait(10, None) == 1
 
 
+def test_misaligned_scale_pointers_are_refused_before_launch(lib):
+    """Every scale pointer is checked like the other tensor pointers: an odd
+    address gets MXFP8_ERR_INVALID_ARG before any launch (no GPU here, so a call
+    that reached a kernel or a device query would return another status)."""
+    P = ctypes.c_void_p
+    fake, odd, odd4 = P(0x10000), P(0x10001), P(0x10004)
+    # pre-quantised activation scales
+    for bad in (odd, odd4):
+        assert lib.mxfp8_linear(None, fake, bad, 1, 300, 256, 512, fake, fake, None, fake, fake,
+                                1 << 20, None) == 1
+        assert b"aligned" in lib.mxfp8_last_error()
+        assert lib.mxfp8_linear_path(3, None, fake, bad, 1, 300, 256, 512, fake, fake, None, fake,
+                                     fake, 1 << 20, None) == 1
+    # weight scales (and the weights) given to the one-time repack
+    assert lib.mxfp8_process_weights(fake, odd4, 1, 8, 128, fake, fake, None) == 1
+    assert lib.mxfp8_process_weights(odd, fake, 1, 8, 128, fake, fake, None) == 1
+    assert lib.mxfp8_process_weights(fake, fake, 1, 8, 128, fake, odd, None) == 1
+    # the standalone scale repack, both sides, and its inverse
+    assert lib.mxfp8_pack_scales(odd4, 1, 8, 128, fake, None) == 1
+    assert lib.mxfp8_pack_scales(fake, 1, 8, 128, odd, None) == 1
+    assert lib.mxfp8_unpack_scales(fake, 1, 8, 128, odd, None) == 1
+    # row-major activation scales written by the standalone quantiser
+    assert lib.mxfp8_quantize(fake, 4, 64, fake, odd, None) == 1
+    assert lib.mxfp8_quantize_packed(fake, 1, 4, 64, fake, odd4, None) == 1
+    # bias and the no-allocation entry point
+    assert lib.mxfp8_linear(fake, None, None, 1, 16, 256, 512, fake, fake, odd, fake, fake,
+                            1 << 20, None) == 1
+    assert lib.mxfp8_linear_noalloc(fake, 1, 16, 256, 512, fake, odd4, None, fake, None) == 1
+
+
+def test_problems_beyond_32_bit_block_indexing_are_unsupported(lib):
+    """The quantise and repack kernels index scale blocks with 32-bit integers:
+    more than 2^31 - 1 blocks is refused with MXFP8_ERR_UNSUPPORTED up front."""
+    fake = ctypes.c_void_p(0x10000)
+    rows, K = 1 << 22, 1 << 14            # 2^22 * 2^9 = 2^31 blocks
+    assert lib.mxfp8_quantize(fake, rows, K, fake, fake, None) == 2
+    assert b"2^31" in lib.mxfp8_last_error()
+    assert lib.mxfp8_quantize_packed(fake, 1, rows, K, fake, fake, None) == 2
+    assert lib.mxfp8_linear(fake, None, None, 1, rows, 256, K, fake, fake, None, fake, fake,
+                            1 << 62, None) == 2
+    assert lib.mxfp8_process_weights(fake, fake, 1, rows, K, fake, fake, None) == 2
+    assert lib.mxfp8_pack_scales(fake, 2, rows // 2, K, fake, None) == 2
+    # one block fewer than the limit is accepted by the size checks (the call
+    # then fails on the missing GPU, not on its arguments)
+    st = lib.mxfp8_quantize(fake, rows - 1, K, fake, fake, None)
+    assert st not in (1, 2)
+
+
 def test_python_binding_validates_shapes():
     with pytest.raises(TypeError):
         ops.quantize(torch.zeros(4, 64, dtype=torch.float32))
