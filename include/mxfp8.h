@@ -249,6 +249,53 @@ mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int64_t M, int6
                                   const void* bias_bf16, void* out_bf16, mxfp8_stream_t stream);
 
 /*
+ * Persistable packed weights.
+ *   Source: the Mxfp8LinearKernel page: supports_pre_processed_weights and the
+ *   weight-cache daemon that hands weights, already processed, to later
+ *   processes, which use them as they are.  The output of
+ *   mxfp8_process_weights depends only on (B, N, K) and on this library's
+ *   layout, so it can be stored once and reloaded without repacking.
+ *   A blob is a 128-byte header (magic "MXFP8PW1", format version, layout id,
+ *   flags, B, N, K, payload sizes, an FNV-1a 64 checksum of the payload and
+ *   one of the header; integers little-endian) followed by the w_packed bytes
+ *   and the sf_packed bytes.  These calls work on HOST memory only (no CUDA
+ *   call, no device memory): the caller copies the payloads between host and
+ *   device (cudaMemcpy or torch).
+ */
+#define MXFP8_BLOB_HEADER_BYTES 128
+
+/* Bytes of the blob for B batches of an [N, K] layer (header + payloads). */
+mxfp8_status mxfp8_blob_size(int64_t B, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * mxfp8_weights_serialize - write a blob.
+ *   w_packed, sf_packed : host, the mxfp8_packed_sizes(B, N, K) bytes of each
+ *                         (as mxfp8_process_weights wrote them, copied to host).
+ *   batched             : 1 if the layer's weights are [B, N, K] (bmm), else 0;
+ *                         stored so that a reader restores the same shapes.
+ *   blob                : host, >= mxfp8_blob_size(B, N, K) bytes, written.
+ *   MXFP8_ERR_INVALID_ARG on a null pointer, a bad shape or a short blob.
+ */
+mxfp8_status mxfp8_weights_serialize(const uint8_t* w_packed, const uint8_t* sf_packed, int64_t B,
+                                     int64_t N, int64_t K, int batched, uint8_t* blob,
+                                     size_t blob_bytes);
+
+/*
+ * mxfp8_weights_deserialize - check a blob and locate its payloads.
+ *   blob, blob_bytes : host, the bytes written by mxfp8_weights_serialize.
+ *   B, N, K, batched : out, the stored shape.
+ *   w_offset, sf_offset : out, byte offsets of the w_packed and sf_packed
+ *                         payloads inside blob (16-byte aligned offsets; the
+ *                         sizes are those of mxfp8_packed_sizes(B, N, K)).
+ *   MXFP8_ERR_INVALID_ARG: null pointer, not a blob, truncated, or either
+ *   checksum wrong (corrupted).  MXFP8_ERR_UNSUPPORTED: written with another
+ *   format version or layout (repack with mxfp8_process_weights instead).
+ *   Nothing is written to the outputs unless the blob is valid.
+ */
+mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, int64_t* B, int64_t* N,
+                                       int64_t* K, int* batched, size_t* w_offset, size_t* sf_offset);
+
+/*
  * mxfp8_check - synchronise `stream`, then read and clear the device status
  * word of the current device.  Returns MXFP8_ERR_TIMEOUT if a bounded wait in
  * any kernel of this library ran out since the last check, MXFP8_ERR_CUDA if

@@ -33,7 +33,8 @@ def _nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    """CUDA translation units (*.cu) and host-only ones (*.cpp, compiled by nvcc's host compiler)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> list[str]:
@@ -67,7 +68,7 @@ def build(force: bool = False, extra_flags: list[str] | None = None) -> str:
     jobs = []
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         for src in sources():
-            obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+            obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
             objs.append(obj)
             jobs.append(ex.submit(_run, [nvcc, *ARCH, *flags, "-c", src, "-o", obj]))
         for j in jobs:

@@ -17,6 +17,7 @@ import ctypes
 import dataclasses
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +46,11 @@ SIGNATURES = {
     "mxfp8_pack_scales": (_INT, [_P, _I64, _I64, _I64, _P, _P]),
     "mxfp8_gemm_packed": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "mxfp8_linear_noalloc": (_INT, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "mxfp8_blob_size": (_INT, [_I64, _I64, _I64, _SIZE_P]),
+    "mxfp8_weights_serialize": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, ctypes.c_size_t]),
+    "mxfp8_weights_deserialize": (_INT, [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.POINTER(ctypes.c_int), _SIZE_P, _SIZE_P]),
     "mxfp8_check": (_INT, [_P]),
     "mxfp8_debug_expire_wait": (_INT, [_U64, _P]),
 }
@@ -170,6 +176,39 @@ def process_weights(w_q: torch.Tensor, w_scale: torch.Tensor) -> PackedWeights:
     _check(load().mxfp8_process_weights(_ptr(_bytes(w_q)), _ptr(_bytes(w_scale)), B, N, K,
                                         _ptr(wp), _ptr(sp), _stream()))
     return PackedWeights(wp, sp, B, N, K, batched)
+
+
+def save_packed(pw: PackedWeights) -> bytes:
+    """The packed weights as one self-describing blob (mxfp8_weights_serialize):
+    a versioned, checksummed header, then the w_packed and sf_packed bytes.
+    Write it to a file once; load_packed restores it without repacking."""
+    w = np.ascontiguousarray(pw.w_packed.detach().cpu().numpy())
+    sf = np.ascontiguousarray(pw.sf_packed.detach().cpu().numpy())
+    n = ctypes.c_size_t()
+    _check(load().mxfp8_blob_size(pw.B, pw.N, pw.K, ctypes.byref(n)))
+    if w.size != packed_sizes(pw.B, pw.N, pw.K)[0] or sf.size != packed_sizes(pw.B, pw.N, pw.K)[1]:
+        raise ValueError("packed tensors do not have the sizes of (B, N, K)")
+    blob = np.empty(n.value, dtype=np.uint8)
+    _check(load().mxfp8_weights_serialize(w.ctypes.data, sf.ctypes.data, pw.B, pw.N, pw.K,
+                                          int(pw.batched), blob.ctypes.data, blob.size))
+    return blob.tobytes()
+
+
+def load_packed(blob: bytes | bytearray | memoryview, device: torch.device | str) -> PackedWeights:
+    """PackedWeights from a blob written by save_packed (checked by
+    mxfp8_weights_deserialize: format, layout, sizes and both checksums),
+    copied to ``device``."""
+    buf = np.frombuffer(blob, dtype=np.uint8)
+    B, N, K = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    batched = ctypes.c_int()
+    wo, so = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().mxfp8_weights_deserialize(buf.ctypes.data, buf.size, ctypes.byref(B), ctypes.byref(N),
+                                            ctypes.byref(K), ctypes.byref(batched), ctypes.byref(wo),
+                                            ctypes.byref(so)))
+    wb, sb = packed_sizes(B.value, N.value, K.value)
+    w = torch.from_numpy(buf[wo.value:wo.value + wb].copy()).to(device)
+    sf = torch.from_numpy(buf[so.value:so.value + sb].copy()).to(device)
+    return PackedWeights(w, sf, B.value, N.value, K.value, bool(batched.value))
 
 
 def unpack_scales(pw: PackedWeights) -> torch.Tensor:
