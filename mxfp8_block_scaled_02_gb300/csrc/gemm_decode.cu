@@ -159,6 +159,11 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The bias of the output column this thread reduces (warps 2.. only): read
+  // before the dependency wait, like the weights (the previous kernel in the
+  // stream never writes it), so its latency is off the path after the MMAs
+  // (measured: 6.27 -> 6.02 us per call at M = 1, 9.80 -> 9.48 at M = 64).
+  float bias_n = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------ weight producer (TMA)
@@ -246,6 +251,11 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         if ((rem & 7) == 0)
           *reinterpret_cast<uint32_t*>(smem + C::OFF_SFX + xs * kAtomBytes + (row & 31) * 16 + (row >> 5) * 4) = 0u;
       }
+    }
+    {
+      const int per = kRows / a.splits;
+      const int n = tile * kRows + static_cast<int>(rank) * per + (threadIdx.x - 64) % per;
+      if (a.bias != nullptr && n < a.N) bias_n = __bfloat162float(a.bias[n]);
     }
     // x is written by the previous kernel in the stream: wait for it to finish.
     grid_dependency_wait();
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     // QTHREADS is a multiple of per, so each thread keeps one output column n
     const int nl = t % per;
     const int n = tile * kRows + static_cast<int>(rank) * per + nl;
-    const float bias = (a.bias != nullptr && n < a.N) ? __bfloat162float(a.bias[n]) : 0.f;
+    const float bias = bias_n;  // loaded before the dependency wait (same n)
     if (n < a.N) {
 #pragma unroll 4
       for (int m = t / per; m < a.M; m += QTHREADS / per) {
