@@ -406,6 +406,8 @@ def run_ours(args):
 
     decode = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 500))
     others = _other_workloads(ops, dev, flush, stream, steps=min(max(n, 10), 100))
+    others["two_layer_mlp_M4096"] = _two_layer_chain(ops, dev, flush, stream, pw, x,
+                                                     steps=min(max(n, 10), 100))
 
     line = None
     if rank == 0:
@@ -565,17 +567,116 @@ def _other_workloads(ops, dev, flush, stream, steps):
     return res
 
 
+def _two_layer_chain(ops, dev, flush, stream, pw_up, x, steps):
+    """A prefill MLP step of two layers, up (M4096 N14336 K4096) then down
+    (M4096 N4096 K14336), with bf16 x: (a) the bf16 chain, where the down
+    layer quantises the up layer's bf16 output with the standalone kernel;
+    (b) the quantised hand-off, where the up layer's epilogue writes its output
+    as MXFP8 codes + packed scales and the down layer reads them directly."""
+    p = synth.prefill_down()
+    p.x = None
+    wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
+    pw_down = ops.process_weights(wq, ws)
+    del wq, ws
+    M = x.shape[0]
+    h = torch.empty((M, pw_up.N), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((1, M, pw_down.N), dtype=torch.bfloat16, device=dev)
+    ws_up = torch.empty(ops.workspace_size(1, M, pw_up.N, pw_up.K, False), dtype=torch.uint8, device=dev)
+    ws_dn = torch.empty(ops.workspace_size(1, M, pw_down.N, pw_down.K, False), dtype=torch.uint8, device=dev)
+    y = ops.PackedActivation(torch.empty((1, M, pw_up.N), dtype=torch.uint8, device=dev),
+                             torch.empty(ops.packed_sizes(1, M, pw_up.N)[1], dtype=torch.uint8, device=dev),
+                             1, M, pw_up.N)
+    lib = ops.load()
+
+    def chain_bf16():
+        ops.linear(x, pw_up, out=h, workspace=ws_up)
+        ops.linear(h, pw_down, out=out[0], workspace=ws_dn)
+
+    def chain_hand_off():
+        ops._check(lib.mxfp8_linear_quantized_out(x.data_ptr(), None, None, 1, M, pw_up.N, pw_up.K,
+                                                  pw_up.w_packed.data_ptr(), pw_up.sf_packed.data_ptr(), None,
+                                                  None, y.x_q.data_ptr(), y.sf_packed.data_ptr(),
+                                                  ws_up.data_ptr(), ws_up.numel(), ops._stream()))
+        ops.gemm_packed(y, pw_down, out=out)
+
+    flops = 2.0 * M * pw_up.K * pw_up.N + 2.0 * M * pw_down.K * pw_down.N
+    res = {}
+    for name, fn in (("bf16_chain", chain_bf16), ("quantized_hand_off", chain_hand_off)):
+        us = _time_steps(fn, flush, stream, steps)
+        res[name] = {"us": us, "tflops": flops / (us * 1e-6) / 1e12}
+    ops.check()
+    res["launches"] = {"bf16_chain": 4, "quantized_hand_off": 3}
+    return res
+
+
+ONLY = ("prefill_up", "prefill_down", "bmm", "decode_M1", "decode_M16", "decode_M64", "chain_hand_off")
+
+
+def run_only(args):
+    """--only WORKLOAD: warm-up, then `steps` calls of one workload with the L2
+    flushed between calls; prints {"only", "us"}.  For profiling runs (ncu
+    launch lists and captures), not the benchmark line."""
+    from mxfp8_block_scaled_02_gb300 import build, ops
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    ops.load()
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    w = args.only
+    if w.startswith("decode_M"):
+        M = int(w[len("decode_M"):])
+        p = synth.decode(64)
+        wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
+        pw = ops.process_weights(wq, ws)
+        x, bias = _dev_bf16(p.x[0, :M], dev), _dev_bf16(p.bias, dev)
+        out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
+        fn = lambda: ops.linear(x, pw, bias, out=out, workspace=wsb)  # noqa: E731
+    elif w == "prefill_down":
+        p = synth.prefill_down()
+        xq, xs = ops.quantize(_dev_bf16(p.x[0], dev))
+        wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
+        pw = ops.process_weights(wq, ws)
+        out = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(ops.workspace_size(1, p.M, p.N, p.K, True), dtype=torch.uint8, device=dev)
+        fn = lambda: ops.linear(xq, pw, x_scale=xs, out=out, workspace=wsb)  # noqa: E731
+    else:
+        p = synth.bmm() if w == "bmm" else synth.prefill_up()
+        x = _dev_bf16(p.x if w == "bmm" else p.x[0], dev)
+        wq, ws = ops.quantize(_dev_bf16(p.w if w == "bmm" else p.w[0], dev))
+        pw = ops.process_weights(wq, ws)
+        out = torch.empty((*x.shape[:-1], p.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(ops.workspace_size(p.B, p.M, p.N, p.K, False), dtype=torch.uint8, device=dev)
+        fn = lambda: ops.linear(x, pw, out=out, workspace=wsb)  # noqa: E731
+        if w == "chain_hand_off":
+            r = _two_layer_chain(ops, dev, flush, stream, pw, x, args.steps)
+            print(json.dumps({"only": w, **r}), flush=True)
+            return
+    for _ in range(args.warmup):
+        fn()
+        flush.zero_()
+    ops.check()
+    t = _time_calls(fn, flush, stream, args.steps)
+    ops.check()
+    print(json.dumps({"only": w, "us": statistics.mean(t) * 1e3, "min_us": min(t) * 1e3}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=ONLY, default=None,
+                    help="time one workload alone (for profiling runs; prints no benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only is not None:
+        run_only(args)
     else:
         run_ours(args)
 

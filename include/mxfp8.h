@@ -218,6 +218,46 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
                                mxfp8_stream_t stream);
 
 /*
+ * mxfp8_linear_quantized_out - mxfp8_linear whose output is handed on to the
+ * next layer already quantised (the QuantizedActivation hand-off).
+ *   Source: "AiterFlyDSLMxfp8LinearKernel.apply_weights" (aiter_flydsl page):
+ *   a layer accepts its input as a QuantizedActivation (data + scale) when the
+ *   previous op produced one, and then skips its own quantise step.  Here the
+ *   GEMM epilogue produces it: y = bf16(x . w^T + bias) exactly as
+ *   mxfp8_linear computes it, quantised by the mxfp8_quantize rule (OCP MX
+ *   v1.0, section 6.3) on the same bf16 bits, so y_q / y_sf_packed are the
+ *   bytes mxfp8_quantize_packed(y) would write (padding rows of the last atom
+ *   tile are left as they were).
+ *   Inputs, w_packed, sf_packed, bias, workspace: as mxfp8_linear (either x
+ *   form; the workspace of mxfp8_workspace_size).
+ *   out_bf16    : device, [B, M, N] bf16 out, or NULL to skip the bf16 output.
+ *   y_q         : device, [B, M, N] E4M3 codes out (16-byte aligned).
+ *   y_sf_packed : device, packed scale atoms of (B, M, N) out, the
+ *                 mxfp8_packed_sizes(B, M, N) sf bytes (16-byte aligned): the
+ *                 activation-scale operand of mxfp8_gemm_packed for the next
+ *                 layer (K = N).
+ *   Requirements as mxfp8_linear, and N % 128 == 0 (the next layer's K;
+ *   else MXFP8_ERR_UNSUPPORTED).  Runs on the large-M GEMM kernels at every M.
+ */
+mxfp8_status mxfp8_linear_quantized_out(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,
+                                        int64_t B, int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
+                                        const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                                        uint8_t* y_q, uint8_t* y_sf_packed, void* workspace,
+                                        size_t workspace_bytes, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_gemm_packed_quantized_out - mxfp8_gemm_packed with the same quantised
+ * hand-off output as mxfp8_linear_quantized_out: the step of a chain of layers
+ * whose input is the previous layer's y_q / y_sf_packed and whose output feeds
+ * the next.  Source and arguments as those two calls (out_bf16 may be NULL;
+ * N % 128 == 0).
+ */
+mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
+                                             int64_t N, int64_t K, const uint8_t* w_packed,
+                                             const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                                             uint8_t* y_q, uint8_t* y_sf_packed, mxfp8_stream_t stream);
+
+/*
  * Size of the fixed device scratch array used by mxfp8_linear_noalloc.
  */
 #define MXFP8_NOALLOC_SCRATCH_BYTES (32ll << 20)

@@ -226,11 +226,36 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, in
   return MXFP8_OK;
 }
 
-mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
-                               const uint8_t* x_scale, int64_t B, int64_t M, int64_t N, int64_t K,
-                               const uint8_t* w_packed, const uint8_t* sf_packed,
-                               const void* bias_bf16, void* out_bf16, void* workspace,
-                               size_t workspace_bytes, mxfp8_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The outputs of a linear call: the bf16 result and/or its MXFP8 quantisation
+// for the next layer (codes [B, M, N] + packed scale atoms of (B, M, N)).
+struct LinearOut {
+  void* out_bf16;
+  uint8_t* y_q;
+  uint8_t* y_sf;
+};
+
+mxfp8_status check_linear_out(const LinearOut& o, int64_t B, int64_t M, int64_t N) {
+  const bool hand_off = o.y_q != nullptr || o.y_sf != nullptr;
+  if (hand_off && (o.y_q == nullptr || o.y_sf == nullptr))
+    return fail(MXFP8_ERR_INVALID_ARG, "y_q and y_sf_packed must both be given");
+  if (o.out_bf16 == nullptr && !hand_off) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  if ((o.out_bf16 != nullptr && !aligned(o.out_bf16, 16)) || (hand_off && (!aligned(o.y_q, 16) || !aligned(o.y_sf, 16))))
+    return fail(MXFP8_ERR_INVALID_ARG, "output pointers must be 16-byte aligned");
+  if (hand_off && N % 128 != 0)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "N=%lld: the quantised output feeds a layer with K = N, which needs N %% 128 == 0", (long long)N);
+  if (hand_off && M > 0) return check_block_count(B, M, N, "quantised output");
+  return MXFP8_OK;
+}
+
+mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale, int64_t B,
+                         int64_t M, int64_t N, int64_t K, const uint8_t* w_packed, const uint8_t* sf_packed,
+                         const void* bias_bf16, const LinearOut& o, void* workspace, size_t workspace_bytes,
+                         mxfp8_stream_t stream) {
   if (path < 0 || path > 3) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
   {
     mxfp8_status ck = check_gemm_args(B, M, N, K);
@@ -243,9 +268,13 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
     return fail(MXFP8_ERR_INVALID_ARG, "pass exactly one of x_bf16 or (x_q, x_scale)");
   if (have_q && (x_q == nullptr || x_scale == nullptr))
     return fail(MXFP8_ERR_INVALID_ARG, "x_q and x_scale must both be given");
-  if (w_packed == nullptr || sf_packed == nullptr || out_bf16 == nullptr)
-    return fail(MXFP8_ERR_INVALID_ARG, "null weight or output pointer");
-  if (!aligned(w_packed, 16) || !aligned(sf_packed, 16) || !aligned(out_bf16, 16) ||
+  if (w_packed == nullptr || sf_packed == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null weight pointer");
+  {
+    mxfp8_status ck = check_linear_out(o, B, M, N);
+    if (ck != MXFP8_OK) return ck;
+  }
+  if (!aligned(w_packed, 16) || !aligned(sf_packed, 16) ||
       (have_x && !aligned(x_bf16, 16)) || (have_q && (!aligned(x_q, 16) || !aligned(x_scale, 16))) ||
       (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
     return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -253,8 +282,11 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
   mxfp8_status st = current_device(&sms);
   if (st != MXFP8_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* out_bf16 = o.out_bf16;
 
-  const bool small_ok = have_x && B == 1 && M <= kSmallM;
+  // the fused small-M kernel has no quantised-output epilogue: the hand-off
+  // always takes the large-M kernels
+  const bool small_ok = have_x && B == 1 && M <= kSmallM && o.y_q == nullptr;
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs bf16 x, B == 1 and M <= %d", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {
@@ -284,11 +316,68 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
     e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
-  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0)};
+  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0),
+                    o.y_q, o.y_sf};
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);
   if (e != cudaSuccess) return cuda_fail(e, msg);
   return MXFP8_OK;
+}
+
+mxfp8_status gemm_packed_impl(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M, int64_t N,
+                              int64_t K, const uint8_t* w_packed, const uint8_t* sf_packed, const void* bias_bf16,
+                              const LinearOut& o, mxfp8_stream_t stream) {
+  mxfp8_status st = check_gemm_args(B, M, N, K);
+  if (st != MXFP8_OK) return st;
+  if (x_q == nullptr || sfa_packed == nullptr || w_packed == nullptr || sf_packed == nullptr)
+    return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
+  if ((st = check_linear_out(o, B, M, N)) != MXFP8_OK) return st;
+  if (!aligned(x_q, 16) || !aligned(sfa_packed, 16) || !aligned(w_packed, 16) || !aligned(sf_packed, 16) ||
+      (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
+    return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (M == 0) return MXFP8_OK;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  mx::GemmProblem p{x_q, w_packed, sfa_packed, sf_packed, bias_bf16, o.out_bf16, B, M, N, K, 0, o.y_q, o.y_sf};
+  const char* msg = "";
+  cudaError_t e = mx::launch_gemm_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream), &msg);
+  if (e != cudaSuccess) return cuda_fail(e, msg);
+  return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
+                               const uint8_t* x_scale, int64_t B, int64_t M, int64_t N, int64_t K,
+                               const uint8_t* w_packed, const uint8_t* sf_packed,
+                               const void* bias_bf16, void* out_bf16, void* workspace,
+                               size_t workspace_bytes, mxfp8_stream_t stream) {
+  if (out_bf16 == nullptr && M != 0) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  return linear_impl(path, x_bf16, x_q, x_scale, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                     LinearOut{out_bf16, nullptr, nullptr}, workspace, workspace_bytes, stream);
+}
+
+mxfp8_status mxfp8_linear_quantized_out(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,
+                                        int64_t B, int64_t M, int64_t N, int64_t K, const uint8_t* w_packed,
+                                        const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                                        uint8_t* y_q, uint8_t* y_sf_packed, void* workspace,
+                                        size_t workspace_bytes, mxfp8_stream_t stream) {
+  if (M != 0 && (y_q == nullptr || y_sf_packed == nullptr))
+    return fail(MXFP8_ERR_INVALID_ARG, "y_q and y_sf_packed are required");
+  return linear_impl(0, x_bf16, x_q, x_scale, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                     LinearOut{out_bf16, y_q, y_sf_packed}, workspace, workspace_bytes, stream);
+}
+
+mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
+                                             int64_t N, int64_t K, const uint8_t* w_packed,
+                                             const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
+                                             uint8_t* y_q, uint8_t* y_sf_packed, mxfp8_stream_t stream) {
+  if (M != 0 && (y_q == nullptr || y_sf_packed == nullptr))
+    return fail(MXFP8_ERR_INVALID_ARG, "y_q and y_sf_packed are required");
+  return gemm_packed_impl(x_q, sfa_packed, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                          LinearOut{out_bf16, y_q, y_sf_packed}, stream);
 }
 
 mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale, int64_t B,
@@ -334,23 +423,9 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
                                int64_t N, int64_t K, const uint8_t* w_packed,
                                const uint8_t* sf_packed, const void* bias_bf16, void* out_bf16,
                                mxfp8_stream_t stream) {
-  mxfp8_status st = check_gemm_args(B, M, N, K);
-  if (st != MXFP8_OK) return st;
-  if (x_q == nullptr || sfa_packed == nullptr || w_packed == nullptr || sf_packed == nullptr ||
-      out_bf16 == nullptr)
-    return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
-  if (!aligned(x_q, 16) || !aligned(sfa_packed, 16) || !aligned(w_packed, 16) ||
-      !aligned(sf_packed, 16) || !aligned(out_bf16, 16) ||
-      (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
-    return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (M == 0) return MXFP8_OK;
-  int sms = 0;
-  if ((st = current_device(&sms)) != MXFP8_OK) return st;
-  mx::GemmProblem p{x_q, w_packed, sfa_packed, sf_packed, bias_bf16, out_bf16, B, M, N, K};
-  const char* msg = "";
-  cudaError_t e = mx::launch_gemm_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream), &msg);
-  if (e != cudaSuccess) return cuda_fail(e, msg);
-  return MXFP8_OK;
+  if (out_bf16 == nullptr && M != 0) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  return gemm_packed_impl(x_q, sfa_packed, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                          LinearOut{out_bf16, nullptr, nullptr}, stream);
 }
 
 mxfp8_status mxfp8_check(mxfp8_stream_t stream) {

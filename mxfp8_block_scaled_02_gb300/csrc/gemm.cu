@@ -36,6 +36,7 @@
 #include <stdint.h>
 
 #include "mx_kernels.h"
+#include "mx_epilogue.cuh"
 #include "mx_layout.cuh"
 #include "mx_ptx.cuh"
 
@@ -82,15 +83,20 @@ struct Cfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory overflow");
   static_assert(BN % 128 == 0 && BN <= 256, "BN");
   static_assert(EPI_COLS % 32 == 0, "epilogue chunks");
+  static_assert(EPI_COLS == 128, "the MXFP8 hand-off quantises 128 columns (one scale word) per thread");
 };
 
 struct Args {
   const uint8_t* sfa;
   const uint8_t* sfb;
   const __nv_bfloat16* bias;
+  uint8_t* yq;   // MXFP8 hand-off outputs (nullptr: none), see mx_epilogue.cuh
+  uint8_t* ysf;
   int B, M, N, K;
   int MT, NT, KT;  // output tiles along M and N, K tiles
   int RTA, RTB;    // 128-row atom tiles of A and of W
+  int RTY, KTY;    // atom tiles of the hand-off scales (rows, K tiles = N / 128)
+  int store_bf16;  // 0: the bf16 output is not written
   int total_tiles;
 };
 
@@ -316,6 +322,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) mbar_arrive(acc_empty);   // accumulator free for the next tile
       acc_phase ^= 1u;
 
+      // the same bf16 values quantised for the next layer (MXFP8 hand-off)
+      if (args.yq != nullptr)
+        store_quantized_row128(packed, args.yq, args.ysf, b, mt * BM + quad * 32 + lane, nt * C::BN + col0,
+                               args.M, args.N, args.RTY, args.KTY);
+      if (!args.store_bf16) continue;
       // registers -> 32 x 32 staging box -> TMA store (rows/columns past M, N are clipped)
 #pragma unroll
       for (int c = 0; c < C::EPI_COLS / 32; ++c) {
@@ -418,13 +429,19 @@ cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stre
   if (e != cudaSuccess) return e;
   e = make_operand_map(&mb, p.w, p.B, p.N, p.K, C::BN, msg);
   if (e != cudaSuccess) return e;
-  e = make_output_map(&mo, p.out, p.B, p.M, p.N, msg);
+  // without a bf16 output the map is never used; any aligned address will do
+  e = make_output_map(&mo, p.out != nullptr ? p.out : static_cast<void*>(p.yq), p.B, p.M, p.N, msg);
   if (e != cudaSuccess) return e;
 
   Args a;
   a.sfa = p.sfa;
   a.sfb = p.sfb;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.yq = p.yq;
+  a.ysf = p.ysf;
+  a.RTY = static_cast<int>(ceil_div(p.M, kAtomRows));
+  a.KTY = static_cast<int>(ceil_div(p.N, kTileK));
+  a.store_bf16 = p.out != nullptr;
   a.B = static_cast<int>(p.B);
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);

@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mx_epilogue.cuh"
 #include "mx_kernels.h"
 #include "mx_layout.cuh"
 #include "mx_ptx.cuh"
@@ -83,14 +84,19 @@ constexpr int P_TMEM_COLS = 512;
 static_assert(P_T_END <= P_TMEM_COLS, "tensor memory overflow");
 static_assert(P_SMEM_ALLOC <= 232448, "shared memory overflow");
 static_assert(PSTAGES % 2 == 0, "scale factors are written per pair of stages");
+static_assert(P_EPI_COLS == 128, "the MXFP8 hand-off quantises 128 columns (one scale word) per thread");
 
 struct PArgs {
   const uint8_t* sfa;
   const uint8_t* sfb;
   const __nv_bfloat16* bias;
+  uint8_t* yq;   // MXFP8 hand-off outputs (nullptr: none), see mx_epilogue.cuh
+  uint8_t* ysf;
   int B, M, N, K;
   int MT2, NT, KT;  // 256-row pair tiles, 256-column tiles, K tiles
   int RTA, RTB;     // 128-row atom tiles of A and of W
+  int RTY, KTY;     // atom tiles of the hand-off scales (rows, K tiles = N / 128)
+  int store_bf16;   // 0: the bf16 output is not written
   int total_tiles;
 };
 
@@ -417,6 +423,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       acc_phase ^= 1u;
 
       const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;
+      // the same bf16 values quantised for the next layer (MXFP8 hand-off)
+      if (args.yq != nullptr)
+        store_quantized_row128(packed, args.yq, args.ysf, b, row0 + lane, nt * PBN + col0, args.M, args.N,
+                               args.RTY, args.KTY);
+      if (!args.store_bf16) continue;
 #pragma unroll
       for (int c = 0; c < P_EPI_COLS / 32; ++c) {
         if (lane == 0 && pending) bulk_wait_group_read0();
@@ -468,13 +479,19 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   if (e != cudaSuccess) return e;
   e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg);
   if (e != cudaSuccess) return e;
-  e = make_output_map(&mo, p.out, p.B, p.M, p.N, msg);
+  // without a bf16 output the map is never used; any aligned address will do
+  e = make_output_map(&mo, p.out != nullptr ? p.out : static_cast<void*>(p.yq), p.B, p.M, p.N, msg);
   if (e != cudaSuccess) return e;
 
   PArgs a;
   a.sfa = p.sfa;
   a.sfb = p.sfb;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.yq = p.yq;
+  a.ysf = p.ysf;
+  a.RTY = static_cast<int>(ceil_div(p.M, kAtomRows));
+  a.KTY = static_cast<int>(ceil_div(p.N, kTileK));
+  a.store_bf16 = p.out != nullptr;
   a.B = static_cast<int>(p.B);
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);

@@ -36,6 +36,11 @@ struct GemmProblem {
   void* out;         // bf16 [B, M, N]
   int64_t B, M, N, K;
   int tiles = 0;     // 0: by M (CTA pairs when M > 128); 1: one CTA per 128 x 256 tile; 2: CTA pairs
+  // MXFP8 hand-off (mx_epilogue.cuh): when yq is set the epilogue also writes
+  // the output quantised, codes [B, M, N] to yq and packed scale atoms of
+  // (B, M, N) to ysf (N % 128 == 0); out may then be nullptr (no bf16 output).
+  uint8_t* yq = nullptr;
+  uint8_t* ysf = nullptr;
 };
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);

@@ -46,6 +46,10 @@ SIGNATURES = {
     "mxfp8_pack_scales": (_INT, [_P, _I64, _I64, _I64, _P, _P]),
     "mxfp8_gemm_packed": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "mxfp8_linear_noalloc": (_INT, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "mxfp8_linear_quantized_out": (_INT, [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P,
+                                          _P, ctypes.c_size_t, _P]),
+    "mxfp8_gemm_packed_quantized_out": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P,
+                                               _P]),
     "mxfp8_blob_size": (_INT, [_I64, _I64, _I64, _SIZE_P]),
     "mxfp8_weights_serialize": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, ctypes.c_size_t]),
     "mxfp8_weights_deserialize": (_INT, [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64),
@@ -328,12 +332,64 @@ def pack_scales(scale: torch.Tensor, B: int = 1) -> torch.Tensor:
 def gemm_packed(pa: PackedActivation, pw: PackedWeights, bias: torch.Tensor | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
     """The block-scaled GEMM + bias epilogue alone; returns bf16 [B, M, N]."""
+    if pa.K != pw.K or pa.B != pw.B:
+        raise ValueError("activation and weights disagree on K or B")
+    _require_cuda(bias, out)
+    if out is not None and (out.dtype != torch.bfloat16 or out.numel() != pa.B * pa.M * pw.N):
+        raise ValueError(f"out must be bf16 with {pa.B * pa.M * pw.N} elements")
     if out is None:
         out = torch.empty((pa.B, pa.M, pw.N), dtype=torch.bfloat16, device=pa.x_q.device)
     _check(load().mxfp8_gemm_packed(_ptr(pa.x_q), _ptr(pa.sf_packed), pa.B, pa.M, pw.N, pa.K,
                                     _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
                                     _stream()))
     return out
+
+
+def _hand_off_buffers(B: int, M: int, N: int, device) -> PackedActivation:
+    y_q = torch.empty((B, M, N), dtype=torch.uint8, device=device)
+    y_sf = torch.empty(packed_sizes(B, max(M, 1), N)[1], dtype=torch.uint8, device=device)
+    return PackedActivation(y_q, y_sf, B, M, N)
+
+
+def linear_quantized_out(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
+                         x_scale: torch.Tensor | None = None, *, bf16_out: bool = True,
+                         workspace: torch.Tensor | None = None
+                         ) -> tuple[torch.Tensor | None, PackedActivation]:
+    """MXFP8 linear layer that also hands its output on quantised
+    (mxfp8_linear_quantized_out): returns (bf16 out or None, y as a
+    PackedActivation that gemm_packed / gemm_packed_quantized_out take as x)."""
+    M = _linear_rows(x, pw, bias, x_scale, None)
+    quantized = x_scale is not None
+    x, x_scale, bias = _aligned16(x), _aligned16(x_scale), _aligned16(bias)
+    out = torch.empty((*x.shape[:-1], pw.N), dtype=torch.bfloat16, device=x.device) if bf16_out else None
+    y = _hand_off_buffers(pw.B, M, pw.N, x.device)
+    if M == 0:
+        return out, y
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(pw.B, M, pw.N, pw.K, quantized), 1), dtype=torch.uint8,
+                                device=x.device)
+    xb = None if quantized else x
+    xq = _bytes(x) if quantized else None
+    _check(load().mxfp8_linear_quantized_out(_ptr(xb), _ptr(xq), _ptr(x_scale), pw.B, M, pw.N, pw.K,
+                                             _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
+                                             _ptr(y.x_q), _ptr(y.sf_packed), _ptr(workspace),
+                                             workspace.numel(), _stream()))
+    return out, y
+
+
+def gemm_packed_quantized_out(pa: PackedActivation, pw: PackedWeights, bias: torch.Tensor | None = None,
+                              *, bf16_out: bool = True) -> tuple[torch.Tensor | None, PackedActivation]:
+    """gemm_packed whose output is also handed on quantised
+    (mxfp8_gemm_packed_quantized_out): the middle layer of a chain."""
+    if pa.K != pw.K or pa.B != pw.B:
+        raise ValueError("activation and weights disagree on K or B")
+    _require_cuda(bias)
+    out = torch.empty((pa.B, pa.M, pw.N), dtype=torch.bfloat16, device=pa.x_q.device) if bf16_out else None
+    y = _hand_off_buffers(pa.B, pa.M, pw.N, pa.x_q.device)
+    _check(load().mxfp8_gemm_packed_quantized_out(_ptr(pa.x_q), _ptr(pa.sf_packed), pa.B, pa.M, pw.N, pa.K,
+                                                  _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
+                                                  _ptr(y.x_q), _ptr(y.sf_packed), _stream()))
+    return out, y
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

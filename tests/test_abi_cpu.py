@@ -120,6 +120,29 @@ def test_misaligned_scale_pointers_are_refused_before_launch(lib):
     assert lib.mxfp8_linear_noalloc(fake, 1, 16, 256, 512, fake, odd4, None, fake, None) == 1
 
 
+def test_quantized_out_argument_errors(lib):
+    """The hand-off calls refuse what they cannot do before any launch."""
+    P = ctypes.c_void_p
+    fake, odd = P(0x10000), P(0x10008)
+    # N % 128 != 0: the hand-off feeds a layer with K = N
+    assert lib.mxfp8_linear_quantized_out(fake, None, None, 1, 300, 136, 512, fake, fake, None, fake, fake, fake,
+                                          fake, 1 << 20, None) == 2
+    assert b"N %" in lib.mxfp8_last_error() or b"128" in lib.mxfp8_last_error()
+    # both hand-off buffers are required; the bf16 output is optional
+    assert lib.mxfp8_linear_quantized_out(fake, None, None, 1, 300, 256, 512, fake, fake, None, fake, None, fake,
+                                          fake, 1 << 20, None) == 1
+    assert lib.mxfp8_gemm_packed_quantized_out(fake, fake, 1, 300, 256, 512, fake, fake, None, None, fake, None,
+                                               None) == 1
+    # misaligned hand-off scale buffer
+    assert lib.mxfp8_linear_quantized_out(fake, None, None, 1, 300, 256, 512, fake, fake, None, None, fake, odd,
+                                          fake, 1 << 20, None) == 1
+    assert lib.mxfp8_gemm_packed_quantized_out(fake, fake, 1, 300, 256, 512, fake, fake, None, None, odd, fake,
+                                               None) == 1
+    # M = 0 is a no-op whatever the pointers
+    assert lib.mxfp8_linear_quantized_out(None, None, None, 1, 0, 256, 512, None, None, None, None, None, None,
+                                          None, 0, None) == 0
+
+
 def test_problems_beyond_32_bit_block_indexing_are_unsupported(lib):
     """The quantise and repack kernels index scale blocks with 32-bit integers:
     more than 2^31 - 1 blocks is refused with MXFP8_ERR_UNSUPPORTED up front."""
