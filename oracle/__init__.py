@@ -7,3 +7,5 @@ library and never imports it.
 
 from .mx_oracle import (BLOCK, block_exponent, dequantize, e4m3_encode, e4m3_value,  # noqa: F401
                         e8m0_value, linear, linear_bf16, quantize, scale_bytes)
+from .mx_oracle import (FP6_FORMATS, fp6_emax, fp6_encode, fp6_max, fp6_value,  # noqa: F401,E402
+                        quantize_fp6)

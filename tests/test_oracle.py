@@ -40,9 +40,9 @@ def _float(s):
     return float(s)
 
 
-def load_golden():
+def load_golden(path=GOLDEN):
     blocks, cur = [], None
-    with open(GOLDEN) as f:
+    with open(path) as f:
         for line in f:
             line = line.strip()
             if not line or line.startswith("#"):
@@ -61,6 +61,8 @@ def load_golden():
                     cur["scale"] = int(toks[0], 16)
                 elif key == "q":
                     cur["q"] = np.array(_expand(toks, lambda t: int(t, 16)), dtype=np.uint8)
+                elif key == "format":
+                    cur["format"] = toks[0]
     return blocks
 
 
