@@ -289,6 +289,58 @@ mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int64_t M, int6
                                   const void* bias_bf16, void* out_bf16, mxfp8_stream_t stream);
 
 /*
+ * MXFP6 weights.
+ *   Source: the mxfp6 page: "MxFp6LinearLayerConfig" (weights quantised per
+ *   block of 32, weight_quant_key kMxfp6E2M3Static or kMxfp6E3M2Static) and
+ *   "MxFp6LinearKernel" (process_weights_after_loading, apply_weights).  The
+ *   element formats are OCP MX v1.0 FP6 (section 5.3.2): E2M3 (bias 1, largest
+ *   7.5, emax 2) and E3M2 (bias 3, largest 28, emax 4), with the same E8M0
+ *   block scales (e = floor(log2 amax) - emax) and MXFP8 activations; the
+ *   tensor cores multiply them directly (kind::mxf8f6f4).
+ *   Packed FP6 weights are 3K/4 bytes per row: every 16 codes of a row are
+ *   12 bytes, code i in bits [6i, 6i + 6) of the little-endian 96-bit group
+ *   (25 % fewer weight bytes than E4M3).  They need K % 128 == 0 and
+ *   w_packed 32-byte aligned.
+ */
+#define MXFP8_WFMT_E4M3 0
+#define MXFP8_WFMT_E2M3 1
+#define MXFP8_WFMT_E3M2 2
+
+/*
+ * mxfp8_quantize_weights - bf16 weights -> w_format codes, one per byte
+ * (E4M3 bytes, or FP6 codes in the low 6 bits), and row-major E8M0 scales
+ * [rows, K/32], by the rule of mxfp8_quantize with the format's emax.  A block
+ * holding Inf or NaN gets scale 0xFF and codes 0x7F (E4M3) or 0x00 (FP6).
+ * Pointers: device, 16-byte aligned; K % 32 == 0.
+ */
+mxfp8_status mxfp8_quantize_weights(const void* w_bf16, int64_t rows, int64_t K, int w_format, uint8_t* w_q,
+                                    uint8_t* w_scale, mxfp8_stream_t stream);
+
+/* mxfp8_packed_sizes for weights of w_format (FP6: 3BNK/4 weight bytes). */
+mxfp8_status mxfp8_packed_sizes_fmt(int w_format, int64_t B, int64_t N, int64_t K, size_t* w_bytes,
+                                    size_t* sf_bytes);
+
+/*
+ * mxfp8_process_weights_fmt - mxfp8_process_weights for w_format weights:
+ * w holds one code per byte ([B, N, K], FP6 codes in the low 6 bits); for
+ * FP6 the codes are packed to 6 bits (w_packed != w, mxfp8_packed_sizes_fmt
+ * bytes, 32-byte aligned).  Scales as mxfp8_process_weights.
+ */
+mxfp8_status mxfp8_process_weights_fmt(int w_format, const uint8_t* w, const uint8_t* w_scale, int64_t B, int64_t N,
+                                       int64_t K, uint8_t* w_packed, uint8_t* sf_packed, mxfp8_stream_t stream);
+
+/*
+ * mxfp8_linear_fmt - mxfp8_linear_path for weights of w_format (packed by
+ * mxfp8_process_weights_fmt with the same format): the block-scaled product
+ * of MXFP8 activations with MXFP6 (or MXFP8) weights.  Arguments and
+ * requirements as mxfp8_linear_path.
+ */
+mxfp8_status mxfp8_linear_fmt(int path, int w_format, const void* x_bf16, const uint8_t* x_q,
+                              const uint8_t* x_scale, int64_t B, int64_t M, int64_t N, int64_t K,
+                              const uint8_t* w_packed, const uint8_t* sf_packed, const void* bias_bf16,
+                              void* out_bf16, void* workspace, size_t workspace_bytes, mxfp8_stream_t stream);
+
+/*
  * Persistable packed weights.
  *   Source: the Mxfp8LinearKernel page: supports_pre_processed_weights and the
  *   weight-cache daemon that hands weights, already processed, to later
@@ -304,36 +356,41 @@ mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int64_t M, int6
  */
 #define MXFP8_BLOB_HEADER_BYTES 128
 
-/* Bytes of the blob for B batches of an [N, K] layer (header + payloads). */
-mxfp8_status mxfp8_blob_size(int64_t B, int64_t N, int64_t K, size_t* bytes);
+/* Bytes of the blob for B batches of an [N, K] layer of w_format weights
+ * (header + payloads). */
+mxfp8_status mxfp8_blob_size(int64_t B, int64_t N, int64_t K, int w_format, size_t* bytes);
 
 /*
  * mxfp8_weights_serialize - write a blob.
- *   w_packed, sf_packed : host, the mxfp8_packed_sizes(B, N, K) bytes of each
- *                         (as mxfp8_process_weights wrote them, copied to host).
+ *   w_packed, sf_packed : host, the mxfp8_packed_sizes_fmt(w_format, B, N, K)
+ *                         bytes of each (as mxfp8_process_weights[_fmt] wrote
+ *                         them, copied to host).
+ *   w_format            : MXFP8_WFMT_*, stored as the layout id (so a reader
+ *                         cannot take packed FP6 bytes for E4M3).
  *   batched             : 1 if the layer's weights are [B, N, K] (bmm), else 0;
  *                         stored so that a reader restores the same shapes.
  *   blob                : host, >= mxfp8_blob_size(B, N, K) bytes, written.
  *   MXFP8_ERR_INVALID_ARG on a null pointer, a bad shape or a short blob.
  */
 mxfp8_status mxfp8_weights_serialize(const uint8_t* w_packed, const uint8_t* sf_packed, int64_t B,
-                                     int64_t N, int64_t K, int batched, uint8_t* blob,
+                                     int64_t N, int64_t K, int w_format, int batched, uint8_t* blob,
                                      size_t blob_bytes);
 
 /*
  * mxfp8_weights_deserialize - check a blob and locate its payloads.
  *   blob, blob_bytes : host, the bytes written by mxfp8_weights_serialize.
- *   B, N, K, batched : out, the stored shape.
+ *   B, N, K, w_format, batched : out, the stored shape and weight format.
  *   w_offset, sf_offset : out, byte offsets of the w_packed and sf_packed
  *                         payloads inside blob (16-byte aligned offsets; the
- *                         sizes are those of mxfp8_packed_sizes(B, N, K)).
+ *                         sizes are those of mxfp8_packed_sizes_fmt).
  *   MXFP8_ERR_INVALID_ARG: null pointer, not a blob, truncated, or either
  *   checksum wrong (corrupted).  MXFP8_ERR_UNSUPPORTED: written with another
  *   format version or layout (repack with mxfp8_process_weights instead).
  *   Nothing is written to the outputs unless the blob is valid.
  */
 mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, int64_t* B, int64_t* N,
-                                       int64_t* K, int* batched, size_t* w_offset, size_t* sf_offset);
+                                       int64_t* K, int* w_format, int* batched, size_t* w_offset,
+                                       size_t* sf_offset);
 
 /*
  * mxfp8_check - synchronise `stream`, then read and clear the device status

@@ -252,11 +252,18 @@ mxfp8_status check_linear_out(const LinearOut& o, int64_t B, int64_t M, int64_t 
   return MXFP8_OK;
 }
 
+mxfp8_status check_wfmt(int w_format) {
+  if (w_format != MXFP8_WFMT_E4M3 && w_format != MXFP8_WFMT_E2M3 && w_format != MXFP8_WFMT_E3M2)
+    return fail(MXFP8_ERR_INVALID_ARG, "w_format=%d", w_format);
+  return MXFP8_OK;
+}
+
 mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale, int64_t B,
                          int64_t M, int64_t N, int64_t K, const uint8_t* w_packed, const uint8_t* sf_packed,
                          const void* bias_bf16, const LinearOut& o, void* workspace, size_t workspace_bytes,
-                         mxfp8_stream_t stream) {
+                         mxfp8_stream_t stream, int w_format = MXFP8_WFMT_E4M3) {
   if (path < 0 || path > 3) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
+  if (check_wfmt(w_format) != MXFP8_OK) return MXFP8_ERR_INVALID_ARG;
   {
     mxfp8_status ck = check_gemm_args(B, M, N, K);
     if (ck != MXFP8_OK) return ck;
@@ -278,6 +285,8 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
       (have_x && !aligned(x_bf16, 16)) || (have_q && (!aligned(x_q, 16) || !aligned(x_scale, 16))) ||
       (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
     return fail(MXFP8_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (w_format != MXFP8_WFMT_E4M3 && !aligned(w_packed, 32))
+    return fail(MXFP8_ERR_INVALID_ARG, "packed FP6 weights must be 32-byte aligned");
   int sms = 0;
   mxfp8_status st = current_device(&sms);
   if (st != MXFP8_OK) return st;
@@ -290,7 +299,7 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs bf16 x, B == 1 and M <= %d", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {
-    mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K};
+    mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K, w_format};
     const char* msg = "";
     cudaError_t e = mx::launch_gemm_decode(p, sms, s, &msg);
     if (e != cudaSuccess) return cuda_fail(e, msg);
@@ -317,7 +326,7 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
     if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
   mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0),
-                    o.y_q, o.y_sf};
+                    o.y_q, o.y_sf, w_format};
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);
   if (e != cudaSuccess) return cuda_fail(e, msg);
@@ -357,6 +366,69 @@ mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
   if (out_bf16 == nullptr && M != 0) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
   return linear_impl(path, x_bf16, x_q, x_scale, B, M, N, K, w_packed, sf_packed, bias_bf16,
                      LinearOut{out_bf16, nullptr, nullptr}, workspace, workspace_bytes, stream);
+}
+
+mxfp8_status mxfp8_linear_fmt(int path, int w_format, const void* x_bf16, const uint8_t* x_q,
+                              const uint8_t* x_scale, int64_t B, int64_t M, int64_t N, int64_t K,
+                              const uint8_t* w_packed, const uint8_t* sf_packed, const void* bias_bf16,
+                              void* out_bf16, void* workspace, size_t workspace_bytes, mxfp8_stream_t stream) {
+  if (out_bf16 == nullptr && M != 0) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  return linear_impl(path, x_bf16, x_q, x_scale, B, M, N, K, w_packed, sf_packed, bias_bf16,
+                     LinearOut{out_bf16, nullptr, nullptr}, workspace, workspace_bytes, stream, w_format);
+}
+
+mxfp8_status mxfp8_quantize_weights(const void* w_bf16, int64_t rows, int64_t K, int w_format, uint8_t* w_q,
+                                    uint8_t* w_scale, mxfp8_stream_t stream) {
+  if (check_wfmt(w_format) != MXFP8_OK) return MXFP8_ERR_INVALID_ARG;
+  if (rows < 0 || K < 1 || K % 32 != 0)
+    return fail(MXFP8_ERR_INVALID_ARG, "rows=%lld K=%lld (K %% 32 == 0)", (long long)rows, (long long)K);
+  if (rows == 0) return MXFP8_OK;
+  if (w_bf16 == nullptr || w_q == nullptr || w_scale == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(w_bf16, 16) || !aligned(w_q, 16) || !aligned(w_scale, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  mxfp8_status st = check_block_count(1, rows, K, "mxfp8_quantize_weights");
+  if (st != MXFP8_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  cudaError_t e = mx::launch_quantize_weights(w_bf16, rows, K, w_format, w_q, w_scale, sms,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "weight quantize launch");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_packed_sizes_fmt(int w_format, int64_t B, int64_t N, int64_t K, size_t* w_bytes,
+                                    size_t* sf_bytes) {
+  if (check_wfmt(w_format) != MXFP8_OK) return MXFP8_ERR_INVALID_ARG;
+  mxfp8_status st = mxfp8_packed_sizes(B, N, K, w_bytes, sf_bytes);
+  if (st != MXFP8_OK) return st;
+  if (w_format != MXFP8_WFMT_E4M3) {
+    if (K % 128 != 0)
+      return fail(MXFP8_ERR_UNSUPPORTED, "K=%lld: packed FP6 weights need K %% 128 == 0", (long long)K);
+    *w_bytes = static_cast<size_t>(B * N * K / 4 * 3);
+  }
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_process_weights_fmt(int w_format, const uint8_t* w, const uint8_t* w_scale, int64_t B, int64_t N,
+                                       int64_t K, uint8_t* w_packed, uint8_t* sf_packed, mxfp8_stream_t stream) {
+  if (check_wfmt(w_format) != MXFP8_OK) return MXFP8_ERR_INVALID_ARG;
+  if (w_format == MXFP8_WFMT_E4M3) return mxfp8_process_weights(w, w_scale, B, N, K, w_packed, sf_packed, stream);
+  mxfp8_status st = check_weights_args(w, w_scale, B, N, K);
+  if (st != MXFP8_OK) return st;
+  if (K % 128 != 0)
+    return fail(MXFP8_ERR_UNSUPPORTED, "K=%lld: packed FP6 weights need K %% 128 == 0", (long long)K);
+  if (w_packed == nullptr || sf_packed == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned(w_packed, 32) || !aligned(sf_packed, 16))
+    return fail(MXFP8_ERR_INVALID_ARG, "w_packed must be 32-byte and sf_packed 16-byte aligned");
+  if (B * N * K / 16 > mx::kMaxBlocks32) return fail(MXFP8_ERR_UNSUPPORTED, "too many FP6 weights for one call");
+  int sms = 0;
+  if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = mx::launch_fp6_pack(w, B * N * K, w_packed, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "FP6 repack launch");
+  e = mx::launch_sf_pack(w_scale, B, N, K, sf_packed, sms, s, false);
+  if (e != cudaSuccess) return cuda_fail(e, "scale repack launch");
+  return MXFP8_OK;
 }
 
 mxfp8_status mxfp8_linear_quantized_out(const void* x_bf16, const uint8_t* x_q, const uint8_t* x_scale,

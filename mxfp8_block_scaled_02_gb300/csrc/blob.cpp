@@ -16,12 +16,14 @@
 // code does not depend on that):
 //     0  8 bytes  magic "MXFP8PW1"
 //     8  u32      format version (1)
-//    12  u32      layout id (1: E4M3 codes K-major + 128x4 scale atoms ordered
-//                 [batch][K tile][row tile], as mx_layout.cuh describes)
+//    12  u32      layout id (1: E4M3 codes K-major; 2 / 3: E2M3 / E3M2 codes
+//                 packed to 6 bits, 3K/4 bytes per row; in all three the
+//                 scales are 128x4 atoms ordered [batch][K tile][row tile], as
+//                 mx_layout.cuh describes)
 //    16  u32      flags (bit 0: the weights were batched, [B, N, K])
 //    20  u32      0
 //    24  i64 B, 32 i64 N, 40 i64 K
-//    48  u64      w_bytes  (= B * N * K)
+//    48  u64      w_bytes  (= B * N * K, or 3BNK/4 for packed FP6)
 //    56  u64      sf_bytes (= the packed scale bytes of (B, N, K))
 //    64  u64      FNV-1a 64 of the payload (w bytes, then sf bytes)
 //    72..119      0
@@ -39,7 +41,9 @@ namespace {
 
 constexpr char kMagic[8] = {'M', 'X', 'F', 'P', '8', 'P', 'W', '1'};
 constexpr uint32_t kFormatVersion = 1;
-constexpr uint32_t kLayoutId = 1;
+// layout id = weight format + 1 (MXFP8_WFMT_*)
+constexpr uint32_t kLayoutE4M3 = 1;
+constexpr uint32_t kLayoutLast = 3;
 constexpr size_t kHeaderBytes = MXFP8_BLOB_HEADER_BYTES;
 
 constexpr uint64_t kFnvOffset = 0xcbf29ce484222325ull;
@@ -75,12 +79,14 @@ mxfp8_status fail(mxfp8_status st, const char* msg) {
   return st;
 }
 
-// Payload sizes for (B, N, K); false if the shape is invalid or too large.
-bool payload_sizes(int64_t B, int64_t N, int64_t K, uint64_t* w, uint64_t* sf) {
+// Payload sizes for (B, N, K) of weight format fmt; false if the shape is
+// invalid or too large.
+bool payload_sizes(int64_t B, int64_t N, int64_t K, int fmt, uint64_t* w, uint64_t* sf) {
   if (B < 1 || N < 1 || K < 1 || K % 32 != 0 || B > (1ll << 20) || N > (1ll << 31) || K > (1ll << 30))
     return false;
   if (B * N > (1ll << 40) || B * N > (INT64_MAX / K)) return false;
-  *w = static_cast<uint64_t>(B * N * K);
+  if (fmt < MXFP8_WFMT_E4M3 || fmt > MXFP8_WFMT_E3M2 || (fmt != MXFP8_WFMT_E4M3 && K % 128 != 0)) return false;
+  *w = static_cast<uint64_t>(fmt == MXFP8_WFMT_E4M3 ? B * N * K : B * N * K / 4 * 3);
   *sf = static_cast<uint64_t>(mx::sf_packed_bytes(B, N, K));
   return true;
 }
@@ -89,22 +95,23 @@ bool payload_sizes(int64_t B, int64_t N, int64_t K, uint64_t* w, uint64_t* sf) {
 
 extern "C" {
 
-mxfp8_status mxfp8_blob_size(int64_t B, int64_t N, int64_t K, size_t* bytes) {
+mxfp8_status mxfp8_blob_size(int64_t B, int64_t N, int64_t K, int w_format, size_t* bytes) {
   uint64_t w = 0, sf = 0;
   if (bytes == nullptr) return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_blob_size: null output pointer");
-  if (!payload_sizes(B, N, K, &w, &sf)) return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_blob_size: bad B, N or K");
+  if (!payload_sizes(B, N, K, w_format, &w, &sf))
+    return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_blob_size: bad B, N, K or w_format");
   *bytes = kHeaderBytes + w + sf;
   return MXFP8_OK;
 }
 
 mxfp8_status mxfp8_weights_serialize(const uint8_t* w_packed, const uint8_t* sf_packed, int64_t B,
-                                     int64_t N, int64_t K, int batched, uint8_t* blob,
+                                     int64_t N, int64_t K, int w_format, int batched, uint8_t* blob,
                                      size_t blob_bytes) {
   uint64_t w = 0, sf = 0;
   if (w_packed == nullptr || sf_packed == nullptr || blob == nullptr)
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_serialize: null pointer");
-  if (!payload_sizes(B, N, K, &w, &sf))
-    return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_serialize: bad B, N or K");
+  if (!payload_sizes(B, N, K, w_format, &w, &sf))
+    return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_serialize: bad B, N, K or w_format");
   if (blob_bytes < kHeaderBytes + w + sf)
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_serialize: blob smaller than mxfp8_blob_size()");
   if (batched != 0 && batched != 1) return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_serialize: batched is 0 or 1");
@@ -112,7 +119,7 @@ mxfp8_status mxfp8_weights_serialize(const uint8_t* w_packed, const uint8_t* sf_
   memset(h, 0, kHeaderBytes);
   memcpy(h, kMagic, 8);
   put_u32(h + 8, kFormatVersion);
-  put_u32(h + 12, kLayoutId);
+  put_u32(h + 12, kLayoutE4M3 + static_cast<uint32_t>(w_format));
   put_u32(h + 16, static_cast<uint32_t>(batched));
   put_u64(h + 24, static_cast<uint64_t>(B));
   put_u64(h + 32, static_cast<uint64_t>(N));
@@ -127,8 +134,9 @@ mxfp8_status mxfp8_weights_serialize(const uint8_t* w_packed, const uint8_t* sf_
 }
 
 mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, int64_t* B, int64_t* N,
-                                       int64_t* K, int* batched, size_t* w_offset, size_t* sf_offset) {
-  if (blob == nullptr || B == nullptr || N == nullptr || K == nullptr || batched == nullptr ||
+                                       int64_t* K, int* w_format, int* batched, size_t* w_offset,
+                                       size_t* sf_offset) {
+  if (blob == nullptr || B == nullptr || N == nullptr || K == nullptr || w_format == nullptr || batched == nullptr ||
       w_offset == nullptr || sf_offset == nullptr)
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_deserialize: null pointer");
   if (blob_bytes < kHeaderBytes)
@@ -138,7 +146,8 @@ mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, i
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_deserialize: not a packed-weights blob (magic)");
   if (get_u64(h + 120) != fnv1a(kFnvOffset, h, 120))
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_deserialize: header checksum mismatch (corrupted)");
-  if (get_u32(h + 8) != kFormatVersion || get_u32(h + 12) != kLayoutId)
+  const uint32_t layout = get_u32(h + 12);
+  if (get_u32(h + 8) != kFormatVersion || layout < kLayoutE4M3 || layout > kLayoutLast)
     return fail(MXFP8_ERR_UNSUPPORTED,
                 "mxfp8_weights_deserialize: blob written with another format version or layout; "
                 "repack the weights with mxfp8_process_weights");
@@ -148,8 +157,9 @@ mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, i
   const int64_t b = static_cast<int64_t>(get_u64(h + 24));
   const int64_t n = static_cast<int64_t>(get_u64(h + 32));
   const int64_t k = static_cast<int64_t>(get_u64(h + 40));
+  const int fmt = static_cast<int>(layout - kLayoutE4M3);
   uint64_t w = 0, sf = 0;
-  if (!payload_sizes(b, n, k, &w, &sf) || get_u64(h + 48) != w || get_u64(h + 56) != sf)
+  if (!payload_sizes(b, n, k, fmt, &w, &sf) || get_u64(h + 48) != w || get_u64(h + 56) != sf)
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_deserialize: sizes do not match (B, N, K)");
   if (blob_bytes < kHeaderBytes + w + sf)
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_weights_deserialize: blob truncated");
@@ -158,6 +168,7 @@ mxfp8_status mxfp8_weights_deserialize(const uint8_t* blob, size_t blob_bytes, i
   *B = b;
   *N = n;
   *K = k;
+  *w_format = fmt;
   *batched = static_cast<int>(flags & 1u);
   *w_offset = kHeaderBytes;
   *sf_offset = kHeaderBytes + w;

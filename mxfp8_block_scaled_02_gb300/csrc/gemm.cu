@@ -39,6 +39,7 @@
 #include "mx_epilogue.cuh"
 #include "mx_layout.cuh"
 #include "mx_ptx.cuh"
+#include "mx_quant.cuh"
 
 namespace mx {
 
@@ -97,6 +98,7 @@ struct Args {
   int RTA, RTB;    // 128-row atom tiles of A and of W
   int RTY, KTY;    // atom tiles of the hand-off scales (rows, K tiles = N / 128)
   int store_bf16;  // 0: the bf16 output is not written
+  int wfmt;        // weight (B operand) element format
   int total_tiles;
 };
 
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bulk_load(smem + C::OFF_SFB + stage * C::SFB_BYTES,
                     args.sfb + (arow * args.RTB + static_cast<int64_t>(nt) * C::NB_ATOMS) * kAtomBytes,
                     nb_atoms * kAtomBytes, &sf_full[stage]);
-          mbar_arrive_expect_tx(&full[stage], C::A_BYTES + C::B_BYTES);
+          mbar_arrive_expect_tx(&full[stage], C::A_BYTES + weight_tile_tx_bytes(C::BN, args.wfmt));
           tma_load_3d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kt * BK, mt * BM, b);
           tma_load_3d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kt * BK,
                       nt * C::BN, b);
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc0 = idesc_mxf8(BM, C::BN);
+      const uint32_t idesc0 = idesc_with_types(idesc_mxf8(BM, C::BN), kFmtE4M3, args.wfmt);
       for (int tile = blockIdx.x; ok && tile < args.total_tiles; tile += gridDim.x) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -386,18 +388,21 @@ cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, i
 // 3-D map over [B][rows][K] bytes, box {128, box_rows, 1}, 128-byte swizzle,
 // zero fill outside the tensor.
 cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
-                             int64_t K, int box_rows, const char** msg) {
+                             int64_t K, int box_rows, const char** msg, int fmt) {
   EncodeTiledFn encode = encode_tiled_fn();
   if (encode == nullptr) {
     *msg = "cuTensorMapEncodeTiled is not available from the driver";
     return cudaErrorNotSupported;
   }
+  // element counts along K; the row stride is in bytes (3K/4 for packed FP6)
+  const int64_t row_bytes = fmt == 0 ? K : K * 3 / 4;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows * K)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows * row_bytes)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims,
+  const CUtensorMapDataType dtype = fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
+  CUresult r = encode(map, dtype, 3, const_cast<uint8_t*>(base), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -427,7 +432,7 @@ cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stre
   CUtensorMap ma, mb, mo;
   cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, BM, msg);
   if (e != cudaSuccess) return e;
-  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, C::BN, msg);
+  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, C::BN, msg, p.wfmt);
   if (e != cudaSuccess) return e;
   // without a bf16 output the map is never used; any aligned address will do
   e = make_output_map(&mo, p.out != nullptr ? p.out : static_cast<void*>(p.yq), p.B, p.M, p.N, msg);
@@ -442,6 +447,7 @@ cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stre
   a.RTY = static_cast<int>(ceil_div(p.M, kAtomRows));
   a.KTY = static_cast<int>(ceil_div(p.N, kTileK));
   a.store_bf16 = p.out != nullptr;
+  a.wfmt = p.wfmt;
   a.B = static_cast<int>(p.B);
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);

@@ -114,6 +114,7 @@ struct Args {
   int KT;      // K / 128
   int RTW;     // 128-row atom tiles of the weights
   int splits;  // cluster size S
+  int wfmt;    // weight (A operand) element format
 };
 
 template <class C>
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         const int st = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
         if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(&full_w[st], kWBytes + kAtomBytes);
+        mbar_arrive_expect_tx(&full_w[st], weight_tile_tx_bytes(kRows, a.wfmt) + kAtomBytes);
         tma_load_3d(smem + C::OFF_W + st * kWBytes, &tmW, &full_w[st], (kt0 + i) * kTK, tile * kRows, 0);
         bulk_load(smem + C::OFF_SFW + st * kAtomBytes,
                   a.sfw + (static_cast<int64_t>(kt0 + i) * a.RTW + tile) * kAtomBytes, kAtomBytes,
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
     if (lane == 0) {
       const int par = warp == 1 ? 0 : 1;
       const uint32_t t_acc = tmem + (par ? C::T_ACC1 : C::T_ACC);
-      const uint32_t idesc0 = idesc_mxf8(kRows, a.n_mma);
+      const uint32_t idesc0 = idesc_with_types(idesc_mxf8(kRows, a.n_mma), a.wfmt, kFmtE4M3);
       bool ok = true;
       for (int i = par; i < nk && ok; i += 2) {
         const int st = i % C::STAGES;
@@ -451,7 +452,7 @@ cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStrea
 
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg) {
   CUtensorMap mw;
-  cudaError_t e = make_operand_map(&mw, p.w, 1, p.N, p.K, kRows, msg);
+  cudaError_t e = make_operand_map(&mw, p.w, 1, p.N, p.K, kRows, msg, p.wfmt);
   if (e != cudaSuccess) return e;
 
   Args a;
@@ -462,6 +463,7 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);
   a.K = static_cast<int>(p.K);
+  a.wfmt = p.wfmt;
   a.n_mma = p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64);  // a power of two: shifts in the quantiser
   a.KT = static_cast<int>(p.K / kTK);
   a.RTW = static_cast<int>(ceil_div(p.N, kAtomRows));

@@ -48,6 +48,7 @@
 #include "mx_kernels.h"
 #include "mx_layout.cuh"
 #include "mx_ptx.cuh"
+#include "mx_quant.cuh"
 
 namespace mx {
 
@@ -97,6 +98,7 @@ struct PArgs {
   int RTA, RTB;     // 128-row atom tiles of A and of W
   int RTY, KTY;     // atom tiles of the hand-off scales (rows, K tiles = N / 128)
   int store_bf16;   // 0: the bf16 output is not written
+  int wfmt;         // weight (B operand) element format
   int total_tiles;
 };
 
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         for (int s0 = 0; s0 < P0; ++s0) {
           const uint32_t full_even = map_shared_rank(smem_u32(&full[s0]), 0);
           if (pass == 0) {
-            if (leader) mbar_arrive_expect_tx(&full[s0], 2 * (P_A_BYTES + P_B_BYTES));
+            if (leader) mbar_arrive_expect_tx(&full[s0], 2 * (P_A_BYTES + weight_tile_tx_bytes(PBN / 2, args.wfmt)));
             tma_load_3d_cluster_bar(smem + P_OFF_B + s0 * P_B_BYTES, &tmB, full_even, kt * PBK,
                                     nt * PBN + static_cast<int>(rank) * (PBN / 2), b);
           } else {
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           // phase early, because this stage was freed by a commit that
           // followed the MMA that waited for the barrier's previous phase.
           const uint32_t full_even = map_shared_rank(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + weight_tile_tx_bytes(PBN / 2, args.wfmt)));
           tma_load_3d_cluster_bar(smem + P_OFF_A + stage * P_A_BYTES, &tmA, full_even, kt * PBK, rt_a * PBM, b);
           tma_load_3d_cluster_bar(smem + P_OFF_B + stage * P_B_BYTES, &tmB, full_even, kt * PBK,
                                   nt * PBN + static_cast<int>(rank) * (PBN / 2), b);
@@ -238,7 +240,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc0 = idesc_mxf8(2 * PBM, PBN);
+      const uint32_t idesc0 = idesc_with_types(idesc_mxf8(2 * PBM, PBN), kFmtE4M3, args.wfmt);
       for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -477,7 +479,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   CUtensorMap ma, mb, mo;
   cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, PBM, msg);
   if (e != cudaSuccess) return e;
-  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg);
+  e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg, p.wfmt);
   if (e != cudaSuccess) return e;
   // without a bf16 output the map is never used; any aligned address will do
   e = make_output_map(&mo, p.out != nullptr ? p.out : static_cast<void*>(p.yq), p.B, p.M, p.N, msg);
@@ -492,6 +494,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   a.RTY = static_cast<int>(ceil_div(p.M, kAtomRows));
   a.KTY = static_cast<int>(ceil_div(p.N, kTileK));
   a.store_bf16 = p.out != nullptr;
+  a.wfmt = p.wfmt;
   a.B = static_cast<int>(p.B);
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);

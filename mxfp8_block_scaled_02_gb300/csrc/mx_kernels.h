@@ -21,6 +21,12 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
                             cudaStream_t stream, bool early_trigger);
 cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
                            int sms, cudaStream_t stream, bool early_trigger);
+// MXFP6 weights: bf16 -> one FP6 (or E4M3) code per byte + row-major scales
+// (fmt: kFmtE4M3 / kFmtE2M3 / kFmtE3M2 of mx_quant.cuh), and the repack of n
+// FP6 codes (n % 16 == 0) into the packed 6-bit layout (3n/4 bytes).
+cudaError_t launch_quantize_weights(const void* x, int64_t rows, int64_t K, int fmt, uint8_t* q, uint8_t* s,
+                                    int sms, cudaStream_t stream);
+cudaError_t launch_fp6_pack(const uint8_t* codes, int64_t n, uint8_t* out, int sms, cudaStream_t stream);
 cudaError_t launch_sf_unpack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,
                              int sms, cudaStream_t stream);
 cudaError_t take_status_quantize(unsigned int* out);
@@ -41,6 +47,7 @@ struct GemmProblem {
   // (B, M, N) to ysf (N % 128 == 0); out may then be nullptr (no bf16 output).
   uint8_t* yq = nullptr;
   uint8_t* ysf = nullptr;
+  int wfmt = 0;      // weight element format: 0 E4M3, 1 E2M3, 2 E3M2 (packed 6-bit, see make_operand_map)
 };
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
@@ -50,9 +57,12 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
 cudaError_t take_status_pair(unsigned int* out);
 // bf16 [B][M][N] output map, box {32 columns, 32 rows, 1} (gemm.cu).
 cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, int64_t N, const char** msg);
-// 3-D TMA map over [B][rows][K] E4M3 bytes, box {128, box_rows, 1}, 128-byte swizzle.
+// 3-D TMA map over [B][rows][K] E4M3 bytes, box {128, box_rows, 1}, 128-byte
+// swizzle.  fmt != 0: the operand is packed 6-bit FP6 codes (3K/4 bytes per
+// row, CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B), which the copy expands to 16
+// bytes per 16 codes in shared memory: the same tile shape as E4M3.
 cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
-                             int64_t K, int box_rows, const char** msg);
+                             int64_t K, int box_rows, const char** msg, int fmt = 0);
 
 // gemm_decode.cu: the small-M path (M <= 64, B = 1, bf16 x): weights on the
 // MMA's M side, activations quantised inside the kernel, split-K across a
@@ -64,6 +74,7 @@ struct DecodeProblem {
   const void* bias;  // bf16 [N] or nullptr
   void* out;         // bf16 [M, N]
   int64_t M, N, K;
+  int wfmt = 0;      // weight element format, as GemmProblem::wfmt
 };
 constexpr int kDecodeMaxM = 64;
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg);

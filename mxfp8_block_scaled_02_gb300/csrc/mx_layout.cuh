@@ -32,6 +32,14 @@ __host__ __device__ __forceinline__ int64_t sf_packed_bytes(int64_t B, int64_t R
   return B * ceil_div(K, kTileK) * ceil_div(R, kAtomRows) * kAtomBytes;
 }
 
+// Bytes one TMA copy of a `rows` x 128-element weight tile counts on its
+// mbarrier: the global bytes it reads, 128 per row for E4M3 and 96 per row
+// for packed 6-bit FP6 codes (wfmt != 0; expanded to 128 bytes per row in
+// shared memory, the same tile shape as E4M3).
+__host__ __device__ __forceinline__ uint32_t weight_tile_tx_bytes(int rows, int wfmt) {
+  return static_cast<uint32_t>(rows) * (wfmt == 0 ? 128u : 96u);
+}
+
 // Offset of the scale of (batch b, row r, block kb) inside the packed buffer.
 __host__ __device__ __forceinline__ int64_t sf_packed_offset(int64_t b, int64_t r, int64_t kb,
                                                             int64_t RT, int64_t KT) {

@@ -271,6 +271,15 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) { return sdesc(sadd
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N) {
   return ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
 }
+// Element type codes of kind::mxf8f6f4 operands (instruction descriptor:
+// A type in bits [7,10), B type in bits [10,13)): E4M3 0, E5M2 1, E2M3 3,
+// E3M2 4, E2M1 5.
+__host__ __device__ constexpr uint32_t mma_type_code(int wfmt) {
+  return wfmt == 1 ? 3u : (wfmt == 2 ? 4u : 0u);
+}
+__host__ __device__ constexpr uint32_t idesc_with_types(uint32_t base, int a_fmt, int b_fmt) {
+  return base | (mma_type_code(a_fmt) << 7) | (mma_type_code(b_fmt) << 10);
+}
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t base, uint32_t sfa_id, uint32_t sfb_id) {
   return base | (sfb_id << 4) | (sfa_id << 29);
 }
@@ -381,6 +390,20 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> two FP6 codes (E2M3 or E3M2), round to nearest even, saturating
+// to the largest finite value; each code in the low 6 bits of its byte, lo in
+// bits [0,8) and hi in bits [8,16).
+__device__ __forceinline__ uint32_t cvt_e2m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e3m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -54,10 +54,31 @@ __device__ __forceinline__ uint32_t quantize_quarter_block(const uint4 v, uint2&
   return sbyte;
 }
 
+// Element formats of a quantised block: kFmtE4M3 for activations and MXFP8
+// weights; kFmtE2M3 / kFmtE3M2 for MXFP6 weights (the mxfp6 page's
+// kMxfp6E2M3Static / kMxfp6E3M2Static), one 6-bit code per byte here.
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtE2M3 = 1;
+constexpr int kFmtE3M2 = 2;
+
+// emax of the element format: floor(log2 of its largest finite value).
+__host__ __device__ constexpr uint32_t fmt_emax(int fmt) { return fmt == kFmtE2M3 ? 2u : (fmt == kFmtE3M2 ? 4u : 8u); }
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fmt_x2(float lo, float hi) {
+  if (FMT == kFmtE2M3) return cvt_e2m3x2(lo, hi);
+  if (FMT == kFmtE3M2) return cvt_e3m2x2(lo, hi);
+  return cvt_e4m3x2(lo, hi);
+}
+
 // One whole 32-element block per lane: 16 bf16 words in, 32 codes (two
 // 16-byte words) and the scale byte out.  The same decisions as
 // quantize_quarter_block, without cross-lane shuffles: a warp quantises 32
-// blocks with ~3x fewer instructions per element.
+// blocks with ~3x fewer instructions per element.  FMT != kFmtE4M3 quantises
+// to an FP6 element instead (scale byte max(E - emax, 0) with that format's
+// emax; a block holding Inf/NaN gets byte 0xFF and codes 0x00, since FP6 has
+// no NaN code).
+template <int FMT = kFmtE4M3>
 __device__ __forceinline__ uint32_t quantize_block32(const uint4 (&v)[4], uint4& c0, uint4& c1) {
   uint32_t w[16];
 #pragma unroll
@@ -76,15 +97,18 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint4 (&v)[4], uint4&
   const uint32_t amax = max(m[0] & 0xFFFFu, m[0] >> 16);
   const bool nonfinite = amax >= 0x7F80u;
   const uint32_t E = amax >> 7;
-  const uint32_t sbyte = nonfinite ? 0xFFu : (E > 8u ? E - 8u : 0u);
+  constexpr uint32_t kEmax = fmt_emax(FMT);
+  const uint32_t sbyte = nonfinite ? 0xFFu : (E > kEmax ? E - kEmax : 0u);
   const float mul = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);
+  constexpr uint32_t kNanCodes = FMT == kFmtE4M3 ? 0x7F7F7F7Fu : 0u;
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t a = cvt_e4m3x2(__uint_as_float(w[2 * i] << 16) * mul, __uint_as_float(w[2 * i] & 0xFFFF0000u) * mul);
-    const uint32_t bb = cvt_e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * mul,
-                                   __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * mul);
-    o[i] = nonfinite ? 0x7F7F7F7Fu : (a | (bb << 16));
+    const uint32_t a = cvt_fmt_x2<FMT>(__uint_as_float(w[2 * i] << 16) * mul,
+                                       __uint_as_float(w[2 * i] & 0xFFFF0000u) * mul);
+    const uint32_t bb = cvt_fmt_x2<FMT>(__uint_as_float(w[2 * i + 1] << 16) * mul,
+                                        __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * mul);
+    o[i] = nonfinite ? kNanCodes : (a | (bb << 16));
   }
   c0 = make_uint4(o[0], o[1], o[2], o[3]);
   c1 = make_uint4(o[4], o[5], o[6], o[7]);

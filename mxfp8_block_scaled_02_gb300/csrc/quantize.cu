@@ -29,7 +29,9 @@ constexpr int kQU = 2;  // 32-block warp tasks per loop iteration, loads all in 
 // stream start at once (griddepcontrol.launch_dependents): only for the
 // quantise step inside the linear layer, whose GEMM reads the codes and scales
 // after its own dependency wait and loads nothing this kernel writes before it.
-template <bool kPacked, bool kEarly>
+// FMT selects the element format (mx_quant.cuh): E4M3, or an FP6 format for
+// MXFP6 weights (row-major scales only).
+template <bool kPacked, bool kEarly, int FMT = kFmtE4M3>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     const uint4* __restrict__ x, uint32_t total_blocks, uint32_t KB, uint8_t* __restrict__ q,
     uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT, uint32_t KT) {
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
       const uint32_t g0 = (t0 + u) * 32;
       const uint32_t g = g0 + lane;
       uint4 c0, c1;
-      const uint32_t sbyte = quantize_block32(v[u], c0, c1);
+      const uint32_t sbyte = quantize_block32<FMT>(v[u], c0, c1);
       if (t0 + u >= ntasks || g >= total_blocks) continue;
       uint4* qd = reinterpret_cast<uint4*>(q + static_cast<uint64_t>(g) * 32);
       qd[0] = c0;
@@ -119,6 +121,29 @@ __global__ void __launch_bounds__(256) sf_pack_kernel(const uint8_t* __restrict_
   }
 }
 
+// FP6 codes, one per byte (low 6 bits) -> the packed 6-bit layout the weight
+// tensor map reads (CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B): every 16
+// consecutive codes of a row become 12 bytes, code i in bits [6i, 6i + 6) of
+// that little-endian 96-bit group, with no gaps; a row of K codes is 3K/4
+// bytes.  One thread per group of 16.
+__global__ void __launch_bounds__(256) fp6_pack_kernel(const uint4* __restrict__ codes, uint32_t* __restrict__ out,
+                                                       uint32_t ngroups) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < ngroups; g += stride) {
+    const uint4 v = __ldg(codes + g);
+    const uint32_t w[4] = {v.x & 0x3F3F3F3Fu, v.y & 0x3F3F3F3Fu, v.z & 0x3F3F3F3Fu, v.w & 0x3F3F3F3Fu};
+    uint32_t c[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i] = (w[i >> 2] >> (8 * (i & 3))) & 0x3Fu;
+    const uint32_t o0 = c[0] | (c[1] << 6) | (c[2] << 12) | (c[3] << 18) | (c[4] << 24) | (c[5] << 30);
+    const uint32_t o1 = (c[5] >> 2) | (c[6] << 4) | (c[7] << 10) | (c[8] << 16) | (c[9] << 22) | (c[10] << 28);
+    const uint32_t o2 = (c[10] >> 4) | (c[11] << 2) | (c[12] << 8) | (c[13] << 14) | (c[14] << 20) | (c[15] << 26);
+    out[3 * static_cast<uint64_t>(g)] = o0;
+    out[3 * static_cast<uint64_t>(g) + 1] = o1;
+    out[3 * static_cast<uint64_t>(g) + 2] = o2;
+  }
+}
+
 // Packed atoms -> row-major [B, R, KB]; one thread per output byte.
 __global__ void __launch_bounds__(256) sf_unpack_kernel(const uint8_t* __restrict__ src, int64_t B,
                                                          int64_t R, int64_t KB, int64_t RT,
@@ -143,12 +168,12 @@ int grid_for(int64_t work_items, int threads, int sms, int per_sm) {
 
 }  // namespace
 
-template <bool kPacked, bool kEarly>
+template <bool kPacked, bool kEarly, int FMT = kFmtE4M3>
 cudaError_t launch_quantize_t(const void* x, int64_t total_blocks, int64_t K, uint8_t* q, uint8_t* s,
                               int64_t rows_per_b, int sms, cudaStream_t stream) {
   static int per_sm = 0;
   if (per_sm == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<kPacked, kEarly>,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<kPacked, kEarly, FMT>,
                                                                   kQuantThreads, 0);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
   }
@@ -156,7 +181,7 @@ cudaError_t launch_quantize_t(const void* x, int64_t total_blocks, int64_t K, ui
   const int grid = grid_for(ceil_div(ntasks, kQU) * 32, kQuantThreads, sms, per_sm);
   const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
   const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
-  quantize_kernel<kPacked, kEarly><<<grid, kQuantThreads, 0, stream>>>(
+  quantize_kernel<kPacked, kEarly, FMT><<<grid, kQuantThreads, 0, stream>>>(
       static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(K / 32), q, s,
       static_cast<uint32_t>(rows_per_b), RT, KT);
   return cudaGetLastError();
@@ -174,6 +199,27 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, 
                          : launch_quantize_t<true, false>(x, total_blocks, K, q, s, rows_per_b, sms, stream);
   return early_trigger ? launch_quantize_t<false, true>(x, total_blocks, K, q, s, rows_per_b, sms, stream)
                        : launch_quantize_t<false, false>(x, total_blocks, K, q, s, rows_per_b, sms, stream);
+}
+
+cudaError_t launch_quantize_weights(const void* x, int64_t rows, int64_t K, int fmt, uint8_t* q, uint8_t* s,
+                                    int sms, cudaStream_t stream) {
+  const int64_t total_blocks = rows * (K / 32);
+  if (total_blocks == 0) return cudaSuccess;
+  if (total_blocks > kMaxBlocks32) return cudaErrorInvalidValue;  // the host refuses these first
+  if (fmt == kFmtE2M3)
+    return launch_quantize_t<false, false, kFmtE2M3>(x, total_blocks, K, q, s, rows, sms, stream);
+  if (fmt == kFmtE3M2)
+    return launch_quantize_t<false, false, kFmtE3M2>(x, total_blocks, K, q, s, rows, sms, stream);
+  return launch_quantize_t<false, false, kFmtE4M3>(x, total_blocks, K, q, s, rows, sms, stream);
+}
+
+cudaError_t launch_fp6_pack(const uint8_t* codes, int64_t n, uint8_t* out, int sms, cudaStream_t stream) {
+  const int64_t ngroups = n / 16;
+  if (ngroups == 0) return cudaSuccess;
+  if (ngroups > kMaxBlocks32) return cudaErrorInvalidValue;  // the host refuses these first
+  fp6_pack_kernel<<<grid_for(ngroups, 256, sms, 8), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(codes), reinterpret_cast<uint32_t*>(out), static_cast<uint32_t>(ngroups));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sf_pack(const uint8_t* src, int64_t B, int64_t R, int64_t K, uint8_t* dst,

@@ -50,16 +50,25 @@ SIGNATURES = {
                                           _P, ctypes.c_size_t, _P]),
     "mxfp8_gemm_packed_quantized_out": (_INT, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P,
                                                _P]),
-    "mxfp8_blob_size": (_INT, [_I64, _I64, _I64, _SIZE_P]),
-    "mxfp8_weights_serialize": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, ctypes.c_size_t]),
+    "mxfp8_blob_size": (_INT, [_I64, _I64, _I64, _INT, _SIZE_P]),
+    "mxfp8_weights_serialize": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _INT, _P, ctypes.c_size_t]),
     "mxfp8_weights_deserialize": (_INT, [_P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int64),
                                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
-                                         ctypes.POINTER(ctypes.c_int), _SIZE_P, _SIZE_P]),
+                                         ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                         _SIZE_P, _SIZE_P]),
+    "mxfp8_quantize_weights": (_INT, [_P, _I64, _I64, _INT, _P, _P, _P]),
+    "mxfp8_packed_sizes_fmt": (_INT, [_INT, _I64, _I64, _I64, _SIZE_P, _SIZE_P]),
+    "mxfp8_process_weights_fmt": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "mxfp8_linear_fmt": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P,
+                                ctypes.c_size_t, _P]),
     "mxfp8_check": (_INT, [_P]),
     "mxfp8_debug_expire_wait": (_INT, [_U64, _P]),
 }
 
 _lib = None
+
+# weight element formats (MXFP8_WFMT_*): E4M3 (MXFP8) and the MXFP6 E2M3 / E3M2
+WFMT = {"e4m3": 0, "e2m3": 1, "e3m2": 2}
 
 
 class MxStatusError(RuntimeError):
@@ -133,26 +142,43 @@ def quantize(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
     return q, s
 
 
-def packed_sizes(B: int, N: int, K: int) -> tuple[int, int]:
+def packed_sizes(B: int, N: int, K: int, fmt: str = "e4m3") -> tuple[int, int]:
     wb, sb = ctypes.c_size_t(), ctypes.c_size_t()
-    _check(load().mxfp8_packed_sizes(B, N, K, ctypes.byref(wb), ctypes.byref(sb)))
+    _check(load().mxfp8_packed_sizes_fmt(WFMT[fmt], B, N, K, ctypes.byref(wb), ctypes.byref(sb)))
     return wb.value, sb.value
+
+
+def quantize_weights(w: torch.Tensor, fmt: str = "e4m3") -> tuple[torch.Tensor, torch.Tensor]:
+    """bf16 weights [..., K] -> (codes uint8 [..., K], one per byte; scales uint8
+    [..., K/32]) in ``fmt`` ("e4m3", or the MXFP6 "e2m3" / "e3m2")."""
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    _require_cuda(w)
+    w = _aligned16(w)
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty((*w.shape[:-1], K // BLOCK), dtype=torch.uint8, device=w.device)
+    _check(load().mxfp8_quantize_weights(_ptr(w), rows, K, WFMT[fmt], _ptr(q), _ptr(s), _stream()))
+    return q, s
 
 
 @dataclasses.dataclass
 class PackedWeights:
     """Weights after the one-time repack: E4M3 bytes and scale atoms."""
 
-    w_packed: torch.Tensor   # uint8, B*N*K bytes
+    w_packed: torch.Tensor   # uint8, B*N*K bytes (3BNK/4 for packed FP6)
     sf_packed: torch.Tensor  # uint8, packed scale atoms
     B: int
     N: int
     K: int
     batched: bool
+    fmt: str = "e4m3"        # weight element format: "e4m3", "e2m3" or "e3m2"
 
 
-def process_weights(w_q: torch.Tensor, w_scale: torch.Tensor) -> PackedWeights:
-    """w_q [N, K] or [B, N, K] (uint8 or float8_e4m3fn), w_scale [..., K/32] uint8.
+def process_weights(w_q: torch.Tensor, w_scale: torch.Tensor, fmt: str = "e4m3") -> PackedWeights:
+    """w_q [N, K] or [B, N, K] (uint8 or float8_e4m3fn; for ``fmt`` "e2m3" /
+    "e3m2" one FP6 code per byte), w_scale [..., K/32] uint8.
 
     A checkpoint may store its scales padded (more rows than N or more blocks
     than K/32, as the aiter_flydsl page's process_weights_after_loading slices
@@ -174,12 +200,12 @@ def process_weights(w_q: torch.Tensor, w_scale: torch.Tensor) -> PackedWeights:
         w_scale = w_scale.contiguous()
     w_q, w_scale = _aligned16(w_q), _aligned16(w_scale)
     _require_cuda(w_q, w_scale)
-    wb, sb = packed_sizes(B, N, K)
+    wb, sb = packed_sizes(B, N, K, fmt)
     wp = torch.empty(wb, dtype=torch.uint8, device=w_q.device)
     sp = torch.empty(sb, dtype=torch.uint8, device=w_q.device)
-    _check(load().mxfp8_process_weights(_ptr(_bytes(w_q)), _ptr(_bytes(w_scale)), B, N, K,
-                                        _ptr(wp), _ptr(sp), _stream()))
-    return PackedWeights(wp, sp, B, N, K, batched)
+    _check(load().mxfp8_process_weights_fmt(WFMT[fmt], _ptr(_bytes(w_q)), _ptr(_bytes(w_scale)), B, N, K,
+                                            _ptr(wp), _ptr(sp), _stream()))
+    return PackedWeights(wp, sp, B, N, K, batched, fmt)
 
 
 def save_packed(pw: PackedWeights) -> bytes:
@@ -189,11 +215,11 @@ def save_packed(pw: PackedWeights) -> bytes:
     w = np.ascontiguousarray(pw.w_packed.detach().cpu().numpy())
     sf = np.ascontiguousarray(pw.sf_packed.detach().cpu().numpy())
     n = ctypes.c_size_t()
-    _check(load().mxfp8_blob_size(pw.B, pw.N, pw.K, ctypes.byref(n)))
-    if w.size != packed_sizes(pw.B, pw.N, pw.K)[0] or sf.size != packed_sizes(pw.B, pw.N, pw.K)[1]:
+    _check(load().mxfp8_blob_size(pw.B, pw.N, pw.K, WFMT[pw.fmt], ctypes.byref(n)))
+    if (w.size, sf.size) != packed_sizes(pw.B, pw.N, pw.K, pw.fmt):
         raise ValueError("packed tensors do not have the sizes of (B, N, K)")
     blob = np.empty(n.value, dtype=np.uint8)
-    _check(load().mxfp8_weights_serialize(w.ctypes.data, sf.ctypes.data, pw.B, pw.N, pw.K,
+    _check(load().mxfp8_weights_serialize(w.ctypes.data, sf.ctypes.data, pw.B, pw.N, pw.K, WFMT[pw.fmt],
                                           int(pw.batched), blob.ctypes.data, blob.size))
     return blob.tobytes()
 
@@ -204,15 +230,16 @@ def load_packed(blob: bytes | bytearray | memoryview, device: torch.device | str
     copied to ``device``."""
     buf = np.frombuffer(blob, dtype=np.uint8)
     B, N, K = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
-    batched = ctypes.c_int()
+    fmt, batched = ctypes.c_int(), ctypes.c_int()
     wo, so = ctypes.c_size_t(), ctypes.c_size_t()
     _check(load().mxfp8_weights_deserialize(buf.ctypes.data, buf.size, ctypes.byref(B), ctypes.byref(N),
-                                            ctypes.byref(K), ctypes.byref(batched), ctypes.byref(wo),
-                                            ctypes.byref(so)))
-    wb, sb = packed_sizes(B.value, N.value, K.value)
+                                            ctypes.byref(K), ctypes.byref(fmt), ctypes.byref(batched),
+                                            ctypes.byref(wo), ctypes.byref(so)))
+    name = {v: k for k, v in WFMT.items()}[fmt.value]
+    wb, sb = packed_sizes(B.value, N.value, K.value, name)
     w = torch.from_numpy(buf[wo.value:wo.value + wb].copy()).to(device)
     sf = torch.from_numpy(buf[so.value:so.value + sb].copy()).to(device)
-    return PackedWeights(w, sf, B.value, N.value, K.value, bool(batched.value))
+    return PackedWeights(w, sf, B.value, N.value, K.value, bool(batched.value), name)
 
 
 def unpack_scales(pw: PackedWeights) -> torch.Tensor:
@@ -284,10 +311,15 @@ def linear(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x.device)
     xb = None if quantized else x
     xq = _bytes(x) if quantized else None
-    _check(load().mxfp8_linear_path(path, _ptr(xb), _ptr(xq), _ptr(x_scale), pw.B, M, pw.N, K,
-                                    _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
-                                    _ptr(workspace), workspace.numel(), _stream()))
+    _check(load().mxfp8_linear_fmt(path, WFMT[pw.fmt], _ptr(xb), _ptr(xq), _ptr(x_scale), pw.B, M, pw.N, K,
+                                   _ptr(pw.w_packed), _ptr(pw.sf_packed), _ptr(bias), _ptr(out),
+                                   _ptr(workspace), workspace.numel(), _stream()))
     return out
+
+
+def _e4m3_only(pw: PackedWeights, what: str) -> None:
+    if pw.fmt != "e4m3":
+        raise ValueError(f"{what} takes E4M3 weights only (these are {pw.fmt}); use linear")
 
 
 @dataclasses.dataclass
@@ -332,6 +364,7 @@ def pack_scales(scale: torch.Tensor, B: int = 1) -> torch.Tensor:
 def gemm_packed(pa: PackedActivation, pw: PackedWeights, bias: torch.Tensor | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
     """The block-scaled GEMM + bias epilogue alone; returns bf16 [B, M, N]."""
+    _e4m3_only(pw, "gemm_packed")
     if pa.K != pw.K or pa.B != pw.B:
         raise ValueError("activation and weights disagree on K or B")
     _require_cuda(bias, out)
@@ -358,6 +391,7 @@ def linear_quantized_out(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor 
     """MXFP8 linear layer that also hands its output on quantised
     (mxfp8_linear_quantized_out): returns (bf16 out or None, y as a
     PackedActivation that gemm_packed / gemm_packed_quantized_out take as x)."""
+    _e4m3_only(pw, "linear_quantized_out")
     M = _linear_rows(x, pw, bias, x_scale, None)
     quantized = x_scale is not None
     x, x_scale, bias = _aligned16(x), _aligned16(x_scale), _aligned16(bias)
@@ -381,6 +415,7 @@ def gemm_packed_quantized_out(pa: PackedActivation, pw: PackedWeights, bias: tor
                               *, bf16_out: bool = True) -> tuple[torch.Tensor | None, PackedActivation]:
     """gemm_packed whose output is also handed on quantised
     (mxfp8_gemm_packed_quantized_out): the middle layer of a chain."""
+    _e4m3_only(pw, "gemm_packed_quantized_out")
     if pa.K != pw.K or pa.B != pw.B:
         raise ValueError("activation and weights disagree on K or B")
     _require_cuda(bias)
@@ -405,6 +440,7 @@ def linear_noalloc(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None
     the GPU share that array and race.  Only ``out`` is allocated here when it
     is not given.
     """
+    _e4m3_only(pw, "linear_noalloc")
     M = _linear_rows(x, pw, bias, None, out)
     K = pw.K
     x, bias = _aligned16(x), _aligned16(bias)
