@@ -408,6 +408,8 @@ def run_ours(args):
     others = _other_workloads(ops, dev, flush, stream, steps=min(max(n, 10), 100))
     others["two_layer_mlp_M4096"] = _two_layer_chain(ops, dev, flush, stream, pw, x,
                                                      steps=min(max(n, 10), 100))
+    others["mxfp6_e2m3_weights"] = _fp6_workloads(ops, dev, flush, stream, x, "e2m3",
+                                                  steps=min(max(n, 10), 100))
 
     line = None
     if rank == 0:
@@ -458,8 +460,9 @@ def run_ours(args):
     return line
 
 
-def _decode_sweep(ops, dev, flush, stream, steps):
-    """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the layer.
+def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64)):
+    """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the layer
+    (weights in ``fmt``: E4M3, or packed MXFP6 with 3/4 of the weight bytes).
 
     Steady state of a decode loop: a CUDA graph of R back-to-back calls, each on
     its own copy of the weights (R copies together exceed twice the L2, so every
@@ -469,20 +472,21 @@ def _decode_sweep(ops, dev, flush, stream, steps):
     """
     p = synth.decode(64)
     w = _dev_bf16(p.w[0], dev)
-    wq, ws = ops.quantize(w)
-    base = ops.process_weights(wq, ws)
+    wq, ws = ops.quantize_weights(w, fmt)
+    base = ops.process_weights(wq, ws, fmt)
     bias = _dev_bf16(p.bias, dev)
     del w, wq, ws
     per_copy = base.w_packed.numel() + base.sf_packed.numel()
     R = int(np.ceil(2 * 129e6 / per_copy)) + 1
     pws = [base] + [ops.PackedWeights(base.w_packed.clone(), base.sf_packed.clone(), base.B, base.N,
-                                      base.K, base.batched) for _ in range(R - 1)]
+                                      base.K, base.batched, base.fmt) for _ in range(R - 1)]
     peaks, _ = _peaks()
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
-    res = {"weight_copies": R, "timing": "CUDA graph of back-to-back calls over rotating weight copies"}
+    res = {"weight_copies": R, "timing": "CUDA graph of back-to-back calls over rotating weight copies",
+           "weights": fmt}
     reps = max(3, min(steps, 200))
     side = torch.cuda.Stream()
-    for M in (1, 4, 16, 64):
+    for M in ms:
         x = _dev_bf16(p.x[0, :M], dev)
         out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
@@ -505,7 +509,7 @@ def _decode_sweep(ops, dev, flush, stream, steps):
         us = a.elapsed_time(b) * 1e3 / (reps * R)
         cold = _time_steps(lambda: ops.linear(x, base, bias, out=out, workspace=wsb), flush, stream,
                            min(steps, 50))
-        nbytes = p.N * p.K + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N + 2 * p.N
+        nbytes = base.w_packed.numel() + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N + 2 * p.N
         res[f"M{M}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
                         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "cold_us": cold,
                         "bytes_per_call": nbytes}
@@ -563,6 +567,23 @@ def _other_workloads(ops, dev, flush, stream, steps):
     res["bmm_B16_M512_N512_K7168"] = {
         "us": us, "tflops": p.flops / (us * 1e-6) / 1e12, "gbs": nbytes / (us * 1e-6) / 1e9,
         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm (x bf16 read once)"}
+    ops.check()
+    return res
+
+
+def _fp6_workloads(ops, dev, flush, stream, x, fmt, steps):
+    """MXFP6 weights (the mxfp6 page's E2M3 / E3M2, packed to 6 bits): the
+    decode sweep (M = 1, 16) and the prefill MLP-up step with the same bf16 x,
+    weights quantised by the library from the same bf16 draws."""
+    res = {"decode": _decode_sweep(ops, dev, flush, stream, steps=max(steps, 20), fmt=fmt, ms=(1, 16))}
+    p = synth.prefill_up()
+    wq, ws = ops.quantize_weights(_dev_bf16(p.w[0], dev), fmt)
+    pw = ops.process_weights(wq, ws, fmt)
+    del wq, ws
+    out = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev)
+    wsb = torch.empty(ops.workspace_size(1, p.M, p.N, p.K, False), dtype=torch.uint8, device=dev)
+    us = _time_steps(lambda: ops.linear(x, pw, out=out, workspace=wsb), flush, stream, steps)
+    res["prefill_up_M4096_N14336_K4096"] = {"us": us, "tflops": p.flops / (us * 1e-6) / 1e12}
     ops.check()
     return res
 
