@@ -410,6 +410,7 @@ def run_ours(args):
                                                      steps=min(max(n, 10), 100))
     others["mxfp6_e2m3_weights"] = _fp6_workloads(ops, dev, flush, stream, x, "e2m3",
                                                   steps=min(max(n, 10), 100))
+    others["medium_m_N4096_K4096"] = _medium_m(ops, dev, flush, stream, steps=min(max(n, 10), 100))
 
     line = None
     if rank == 0:
@@ -567,6 +568,30 @@ def _other_workloads(ops, dev, flush, stream, steps):
     res["bmm_B16_M512_N512_K7168"] = {
         "us": us, "tflops": p.flops / (us * 1e-6) / 1e12, "gbs": nbytes / (us * 1e-6) / 1e9,
         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm (x bf16 read once)"}
+    ops.check()
+    return res
+
+
+def _medium_m(ops, dev, flush, stream, steps):
+    """Prefill chunks of 128 / 256 / 512 tokens at N = K = 4096 (bf16 x, one
+    call after an L2 flush): few output tiles, so the library splits K over CTA
+    pairs; the unsplit CTA-pair path (path 3) beside it."""
+    p = synth.decode(64)       # N = K = 4096 weights and bias of the decode workload
+    wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
+    pw = ops.process_weights(wq, ws)
+    bias = _dev_bf16(p.bias, dev)
+    res = {}
+    for M in (128, 256, 512):
+        x = _dev_bf16(synth.to_bf16_bits(synth.normal(77 + M, M * p.K)).reshape(M, p.K), dev)
+        out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
+        wsb = torch.empty(ops.workspace_size(1, M, p.N, p.K, False), dtype=torch.uint8, device=dev)
+        flops = 2.0 * M * p.N * p.K
+        r = {}
+        for name, path in (("split_k", 0), ("unsplit_pairs", 3)):
+            us = _time_steps(lambda: ops.linear(x, pw, bias, out=out, workspace=wsb, path=path), flush, stream,
+                             steps)
+            r[name] = {"us": us, "tflops": flops / (us * 1e-6) / 1e12}
+        res[f"M{M}"] = r
     ops.check()
     return res
 

@@ -121,7 +121,9 @@ mxfp8_status mxfp8_unpack_scales(const uint8_t* sf_packed, int64_t B, int64_t N,
 
 /*
  * mxfp8_workspace_size - device workspace bytes mxfp8_linear needs for this
- * problem.  x_is_quantized = 1 when the caller passes x_q/x_scale.
+ * problem (the quantised activations and their packed scales, plus the
+ * split-K partials, 4 * splits * B * M * N bytes, when the shape is split).
+ * x_is_quantized = 1 when the caller passes x_q/x_scale.
  */
 mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
                                   int x_is_quantized, size_t* bytes);
@@ -174,9 +176,14 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * path with one CTA per 128 x 256 output tile (separate quantise kernel, then
  * the GEMM), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
  * cta_group::2; what path 0 takes for M > 128 when the small-M path does not
- * apply).  All paths
- * compute the same function; this exists so that tests can check each on
- * every shape.  Path 1 needs M <= 64 and x_bf16 (else MXFP8_ERR_UNSUPPORTED).
+ * apply), 4 = the large-M kernels chosen as path 0 chooses them, never the
+ * small-M one (CTA pairs with split-K when the shape has at most 16
+ * 256 x 256 output tiles: each tile's K range is split over several pairs,
+ * fp32 partials go to the workspace and are added in a fixed order, so the
+ * result is the same on every call; this is also what the quantised hand-off
+ * uses).  All paths compute the same function; this exists so that tests can
+ * check each on every shape.  Path 1 needs M <= 64 and x_bf16 (else
+ * MXFP8_ERR_UNSUPPORTED).
  */
 mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
                                const uint8_t* x_scale, int64_t B, int64_t M, int64_t N,

@@ -76,16 +76,21 @@ int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 constexpr int kSmallM = mx::kDecodeMaxM;  // largest M the fused small-M path serves
 
 struct WsLayout {
-  int64_t xq_off, xq_bytes, sfa_off, sfa_bytes, total;
+  int64_t xq_off, xq_bytes, sfa_off, sfa_bytes, part_off, part_bytes, total;
 };
 
-WsLayout prefill_workspace(int64_t B, int64_t M, int64_t K, bool quantized) {
+// Workspace of a large-M call: quantised activations (bf16 input only), their
+// packed scales, then the split-K partials (fp32 [splits * B][M][N]) when the
+// shape is split.
+WsLayout prefill_workspace(int64_t B, int64_t M, int64_t N, int64_t K, bool quantized, int splits) {
   WsLayout w;
   w.xq_off = 0;
   w.xq_bytes = quantized ? 0 : round_up(B * M * K, 256);
   w.sfa_off = w.xq_bytes;
   w.sfa_bytes = round_up(mx::sf_packed_bytes(B, M, K), 256);
-  w.total = w.xq_bytes + w.sfa_bytes;
+  w.part_off = w.sfa_off + w.sfa_bytes;
+  w.part_bytes = splits > 1 ? round_up(static_cast<int64_t>(splits) * B * M * N * 4, 256) : 0;
+  w.total = w.part_off + w.part_bytes;
   return w;
 }
 
@@ -222,7 +227,9 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K, in
   if (B < 1 || M < 0 || N < 1 || K < 1 || K % 32 != 0)
     return fail(MXFP8_ERR_INVALID_ARG, "B=%lld M=%lld N=%lld K=%lld", (long long)B, (long long)M,
                 (long long)N, (long long)K);
-  *bytes = static_cast<size_t>(prefill_workspace(B, M, K, x_is_quantized != 0).total);
+  if (B * M > (1ll << 31) || N > (1ll << 30) || K > (1ll << 30))
+    return fail(MXFP8_ERR_UNSUPPORTED, "problem too large");
+  *bytes = static_cast<size_t>(prefill_workspace(B, M, N, K, x_is_quantized != 0, mx::splitk_splits(B, M, N, K)).total);
   return MXFP8_OK;
 }
 
@@ -262,7 +269,7 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
                          int64_t M, int64_t N, int64_t K, const uint8_t* w_packed, const uint8_t* sf_packed,
                          const void* bias_bf16, const LinearOut& o, void* workspace, size_t workspace_bytes,
                          mxfp8_stream_t stream, int w_format = MXFP8_WFMT_E4M3) {
-  if (path < 0 || path > 3) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
+  if (path < 0 || path > 4) return fail(MXFP8_ERR_INVALID_ARG, "path=%d", path);
   if (check_wfmt(w_format) != MXFP8_OK) return MXFP8_ERR_INVALID_ARG;
   {
     mxfp8_status ck = check_gemm_args(B, M, N, K);
@@ -306,7 +313,9 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
     return MXFP8_OK;
   }
 
-  const WsLayout ws = prefill_workspace(B, M, K, have_q);
+  // paths 0 and 4 split K over CTA pairs when the shape has few output tiles
+  const int splits = (path == 0 || path == 4) ? mx::splitk_splits(B, M, N, K) : 1;
+  const WsLayout ws = prefill_workspace(B, M, N, K, have_q, splits);
   if (static_cast<int64_t>(workspace_bytes) < ws.total)
     return fail(MXFP8_ERR_INVALID_ARG, "workspace has %zu bytes, needs %lld", workspace_bytes,
                 (long long)ws.total);
@@ -327,6 +336,10 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   }
   mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0),
                     o.y_q, o.y_sf, w_format};
+  if (splits > 1) {
+    p.part = reinterpret_cast<float*>(wsb + ws.part_off);
+    p.splits = splits;
+  }
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);
   if (e != cudaSuccess) return cuda_fail(e, msg);

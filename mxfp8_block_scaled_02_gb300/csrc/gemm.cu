@@ -385,6 +385,26 @@ cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, i
   return cudaSuccess;
 }
 
+cudaError_t make_partial_map(CUtensorMap* map, float* part, int64_t Z, int64_t M, int64_t N, const char** msg) {
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) {
+    *msg = "cuTensorMapEncodeTiled is not available from the driver";
+    return cudaErrorNotSupported;
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(Z)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N * 4), static_cast<cuuint64_t>(M * N * 4)};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *msg = "cuTensorMapEncodeTiled rejected the split-K partials";
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 // 3-D map over [B][rows][K] bytes, box {128, box_rows, 1}, 128-byte swizzle,
 // zero fill outside the tensor.
 cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
@@ -415,7 +435,8 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, i
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
   // 256 x 256 tiles on CTA pairs load 32 KB per SM and K tile against 48 KB
   // for 128 x 256 tiles on one CTA, and measure faster once M spans a pair tile.
-  if (p.tiles == 2 || (p.tiles == 0 && p.M > 128 && sms >= 2)) return launch_gemm_pair(p, sms, stream, msg);
+  if (p.tiles == 2 || (p.tiles == 0 && (p.M > 128 || (p.part != nullptr && p.splits > 1)) && sms >= 2))
+    return launch_gemm_pair(p, sms, stream, msg);
   using C = PrefillCfg;
   static bool attr_set[64] = {};
   int dev = 0;

@@ -100,6 +100,8 @@ struct PArgs {
   int store_bf16;   // 0: the bf16 output is not written
   int wfmt;         // weight (B operand) element format
   int total_tiles;
+  int splits;       // K splits per tile (split-K): > 1 writes fp32 partials through tmPart
+  int units;        // total_tiles * splits
 };
 
 __device__ __forceinline__ void pair_tile_coords(int tile, const PArgs& a, int& b, int& mt2, int& nt) {
@@ -110,9 +112,31 @@ __device__ __forceinline__ void pair_tile_coords(int tile, const PArgs& a, int& 
   mt2 = t - nt * a.MT2;
 }
 
+// Work unit u = tile * splits + s: output tile `tile`, K tiles [kt_lo, kt_hi)
+// (the splits of one tile go to consecutive pairs, which run them at once).
+__device__ __forceinline__ void unit_coords(int u, const PArgs& a, int& b, int& mt2, int& nt, int& s, int& kt_lo,
+                                            int& kt_hi) {
+  const int tile = u / a.splits;
+  s = u - tile * a.splits;
+  pair_tile_coords(tile, a, b, mt2, nt);
+  kt_lo = s * a.KT / a.splits;
+  kt_hi = (s + 1) * a.KT / a.splits;
+}
+
+// K steps (stages) of all units pair `pair` runs.
+__device__ __forceinline__ int64_t pair_steps(int pair, int npairs, const PArgs& a) {
+  int64_t n = 0;
+  for (int u = pair; u < a.units; u += npairs) {
+    const int s = u % a.splits;
+    n += (s + 1) * a.KT / a.splits - s * a.KT / a.splits;
+  }
+  return n;
+}
+
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmOut, const PArgs args) {
+                          const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPart,
+                          const PArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_OFF_BAR);
@@ -144,6 +168,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmOut);
+    if (args.splits > 1) prefetch_tmap(&tmPart);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
@@ -162,11 +187,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       // do not depend on the kernel before this one in the stream, the
       // activation tiles (its output) do.  Issue the weights, wait for the
       // dependency (programmatic dependent launch), then the activations.
-      const int my_tiles = pair < args.total_tiles ? (args.total_tiles - 1 - pair) / npairs + 1 : 0;
-      const int P0 = static_cast<int>(min(static_cast<int64_t>(PSTAGES), static_cast<int64_t>(my_tiles) * args.KT));
+      const int P0 = static_cast<int>(min(static_cast<int64_t>(PSTAGES), pair_steps(pair, npairs, args)));
       for (int pass = 0; pass < 2; ++pass) {
-        int tile = pair, kt = 0, b = 0, mt2 = 0, nt = 0;
-        if (P0 > 0) pair_tile_coords(tile, args, b, mt2, nt);
+        int u = pair, kt = 0, kt_hi = 0, b = 0, mt2 = 0, nt = 0, sp = 0;
+        if (P0 > 0) unit_coords(u, args, b, mt2, nt, sp, kt, kt_hi);
         for (int s0 = 0; s0 < P0; ++s0) {
           const uint32_t full_even = map_shared_rank(smem_u32(&full[s0]), 0);
           if (pass == 0) {
@@ -177,10 +201,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             tma_load_3d_cluster_bar(smem + P_OFF_A + s0 * P_A_BYTES, &tmA, full_even, kt * PBK,
                                     (mt2 * 2 + static_cast<int>(rank)) * PBM, b);
           }
-          if (++kt == args.KT) {
-            kt = 0;
-            tile += npairs;
-            if (tile < args.total_tiles) pair_tile_coords(tile, args, b, mt2, nt);
+          if (++kt == kt_hi) {
+            u += npairs;
+            if (u < args.units) unit_coords(u, args, b, mt2, nt, sp, kt, kt_hi);
           }
         }
         if (pass == 0) grid_dependency_wait();
@@ -189,11 +212,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
-        int b, mt2, nt;
-        pair_tile_coords(tile, args, b, mt2, nt);
+      for (int u = pair; ok && u < args.units; u += npairs) {
+        int b, mt2, nt, sp, kt_lo, kt_hi;
+        unit_coords(u, args, b, mt2, nt, sp, kt_lo, kt_hi);
         const int rt_a = mt2 * 2 + static_cast<int>(rank);  // this CTA's activation row tile
-        for (int kt = 0; kt < args.KT; ++kt) {
+        for (int kt = kt_lo; kt < kt_hi; ++kt) {
           if (issued < P0) {  // issued by the prologue
             ++issued;
             if (++stage == PSTAGES) {
@@ -241,13 +264,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t idesc0 = idesc_with_types(idesc_mxf8(2 * PBM, PBN), kFmtE4M3, args.wfmt);
-      for (int tile = pair; ok && tile < args.total_tiles; tile += npairs) {
+      for (int u = pair; ok && u < args.units; u += npairs) {
+        const int sp = u % args.splits;
+        const int kt_lo = sp * args.KT / args.splits, kt_hi = (sp + 1) * args.KT / args.splits;
         if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < args.KT; ++kt) {
+        for (int kt = kt_lo; kt < kt_hi; ++kt) {
           // operands of both CTAs landed, and both CTAs' scales are in TMEM
           // one wait per pair of stages: the even CTA's scale writers arrive on
           // sf_ready only after both stages' operands have landed
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < PBK / 32; ++kk)
             tc_mma_mxf8_pair(tmem + P_T_ACC, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc0, kk, kk),
-                             t_sfa, t_sfb, (kt | kk) != 0);
+                             t_sfa, t_sfb, ((kt - kt_lo) | kk) != 0);
           tc_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == PSTAGES) {
             stage = 0;
@@ -286,23 +311,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t ready_even = map_shared_rank(smem_u32(sf_ready), 0);
     grid_dependency_wait();  // the activation scales are the previous kernel's output
-    const int my_tiles = pair < args.total_tiles ? (args.total_tiles - 1 - pair) / npairs + 1 : 0;
-    const int64_t total = static_cast<int64_t>(my_tiles) * args.KT;
+    const int64_t total = pair_steps(pair, npairs, args);
     // Fetch cursor: pointers to this lane's line of the activation atom and
-    // of the first weight atom of K tile f_kt of tile f_tile; advancing a K
+    // of the first weight atom of K tile f_kt of unit f_u; advancing a K
     // tile adds one K-tile row of atoms.
-    int f_tile = pair, f_kt = 0;
+    int f_u = pair, f_kt = 0, f_kt_hi = 0;
     const uint8_t* f_a = nullptr;
     const uint8_t* f_w = nullptr;
     bool f_has_a = false, f_has_w1 = false;
     const int64_t a_step = static_cast<int64_t>(args.RTA) * kAtomBytes;
     const int64_t w_step = static_cast<int64_t>(args.RTB) * kAtomBytes;
     auto start_tile = [&]() {
-      if (f_tile >= args.total_tiles) return;
-      int b, mt2, nt;
-      pair_tile_coords(f_tile, args, b, mt2, nt);
+      if (f_u >= args.units) return;
+      int b, mt2, nt, sp;
+      unit_coords(f_u, args, b, mt2, nt, sp, f_kt, f_kt_hi);
       const int rt_a = mt2 * 2 + static_cast<int>(rank);
-      const int64_t arow = static_cast<int64_t>(b) * args.KT;
+      const int64_t arow = static_cast<int64_t>(b) * args.KT + f_kt;
       f_has_a = rt_a < args.RTA;
       f_has_w1 = 2 * nt + 1 < args.RTB;
       f_a = args.sfa + (arow * args.RTA + (f_has_a ? rt_a : 0)) * kAtomBytes + lane * 16;
@@ -316,9 +340,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       vb1 = f_has_w1 ? __ldg(reinterpret_cast<const uint4*>(f_w + kAtomBytes)) : zero;
       f_a += a_step;
       f_w += w_step;
-      if (++f_kt == args.KT) {
-        f_kt = 0;
-        f_tile += npairs;
+      if (++f_kt == f_kt_hi) {
+        f_u += npairs;
         start_tile();
       }
     };
@@ -384,11 +407,46 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const uint32_t acc_empty_even = map_shared_rank(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     bool pending = false;
-    for (int tile = pair; tile < args.total_tiles; tile += npairs) {
-      int b, mt2, nt;
-      pair_tile_coords(tile, args, b, mt2, nt);
+    for (int u = pair; u < args.units; u += npairs) {
+      int b, mt2, nt, sp, kt_lo, kt_hi;
+      unit_coords(u, args, b, mt2, nt, sp, kt_lo, kt_hi);
       if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
+      const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;
+      if (args.splits > 1) {
+        // split-K: this unit's fp32 partial, no bias, through 32-row x
+        // 16-column boxes into the workspace [splits * B][M][N] at
+        // z = split * B + b (rows / columns past M, N are clipped); the
+        // reduce kernel adds the partials in split order
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + P_T_ACC + col0;
+        for (int c = 0; c < P_EPI_COLS / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (lane == 0 && pending) bulk_wait_group_read0();
+            __syncwarp();
+            uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 64);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(r[16 * h + 4 * q], r[16 * h + 4 * q + 1], r[16 * h + 4 * q + 2],
+                                  r[16 * h + 4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmPart, stage_out, nt * PBN + col0 + c * 32 + 16 * h, row0, sp * args.B + b);
+              bulk_commit_group();
+              pending = true;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc_empty_even);
+        acc_phase ^= 1u;
+        continue;
+      }
       uint32_t packed[P_EPI_COLS / 2];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + P_T_ACC + col0;
 #pragma unroll
@@ -424,7 +482,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (lane == 0) mbar_arrive_remote(acc_empty_even);  // the even CTA may start the next tile
       acc_phase ^= 1u;
 
-      const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;
       // the same bf16 values quantised for the next layer (MXFP8 hand-off)
       if (args.yq != nullptr)
         store_quantized_row128(packed, args.yq, args.ysf, b, row0 + lane, nt * PBN + col0, args.M, args.N,
@@ -476,14 +533,23 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
     }
     attr_set[dev] = true;
   }
-  CUtensorMap ma, mb, mo;
+  CUtensorMap ma, mb, mo, mp;
   cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, PBM, msg);
   if (e != cudaSuccess) return e;
   e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg, p.wfmt);
   if (e != cudaSuccess) return e;
-  // without a bf16 output the map is never used; any aligned address will do
-  e = make_output_map(&mo, p.out != nullptr ? p.out : static_cast<void*>(p.yq), p.B, p.M, p.N, msg);
+  const int splits = p.part != nullptr && p.splits > 1 ? p.splits : 1;
+  // without a bf16 output (hand-off only, or split-K partials) the map is never
+  // used; any aligned address will do
+  void* out_any = p.out != nullptr ? p.out : (p.yq != nullptr ? static_cast<void*>(p.yq) : static_cast<void*>(p.part));
+  e = make_output_map(&mo, out_any, p.B, p.M, p.N, msg);
   if (e != cudaSuccess) return e;
+  if (splits > 1) {
+    e = make_partial_map(&mp, p.part, static_cast<int64_t>(splits) * p.B, p.M, p.N, msg);
+    if (e != cudaSuccess) return e;
+  } else {
+    mp = mo;  // unused
+  }
 
   PArgs a;
   a.sfa = p.sfa;
@@ -505,7 +571,15 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   a.RTA = static_cast<int>(ceil_div(p.M, kAtomRows));
   a.RTB = static_cast<int>(ceil_div(p.N, kAtomRows));
   a.total_tiles = a.B * a.MT2 * a.NT;
-  const int pairs = a.total_tiles < sms / 2 ? a.total_tiles : sms / 2;
+  a.splits = splits;
+  a.units = a.total_tiles * splits;
+  // split-K: the partials carry no bias and no hand-off; the reduce adds them
+  if (splits > 1) {
+    a.bias = nullptr;
+    a.yq = a.ysf = nullptr;
+    a.store_bf16 = 0;
+  }
+  const int pairs = a.units < sms / 2 ? a.units : sms / 2;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
@@ -523,8 +597,15 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, a);
-  if (e != cudaSuccess) *msg = "pair GEMM launch failed";
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, mp, a);
+  if (e != cudaSuccess) {
+    *msg = "pair GEMM launch failed";
+    return e;
+  }
+  if (splits > 1) {
+    e = launch_splitk_reduce(p.part, splits, p.B, p.M, p.N, p.bias, p.out, p.yq, p.ysf, sms, stream);
+    if (e != cudaSuccess) *msg = "split-K reduce launch failed";
+  }
   return e;
 }
 

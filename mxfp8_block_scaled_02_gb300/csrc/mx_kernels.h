@@ -48,7 +48,23 @@ struct GemmProblem {
   uint8_t* yq = nullptr;
   uint8_t* ysf = nullptr;
   int wfmt = 0;      // weight element format: 0 E4M3, 1 E2M3, 2 E3M2 (packed 6-bit, see make_operand_map)
+  // split-K (CTA-pair kernel only): with part set and splits > 1, each tile's K
+  // range is split over `splits` pairs, the fp32 partials go to part
+  // ([splits * B][M][N]) and a reduce kernel writes out / the hand-off.
+  float* part = nullptr;
+  int splits = 1;
 };
+// K splits the linear layer uses for a shape (1 = none): enough to give about
+// 64 CTA pairs work when there are at most 16 tiles of 256 x 256, with at least
+// four 128-wide K tiles per split and at most 8 splits.  A function of the
+// shape alone, so the workspace size is known before the call.
+int splitk_splits(int64_t B, int64_t M, int64_t N, int64_t K);
+// out[b, m, n] = bf16(sum over s of part[s][b][m][n] in order s = 0.. + bias[n]),
+// and / or the MXFP8 hand-off of those bf16 values (splitk.cu).
+cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t B, int64_t M, int64_t N, const void* bias,
+                                 void* out, uint8_t* yq, uint8_t* ysf, int sms, cudaStream_t stream);
+// fp32 [Z][M][N] split-K partials, box {16 columns, 32 rows, 1} (gemm.cu).
+cudaError_t make_partial_map(CUtensorMap* map, float* part, int64_t Z, int64_t M, int64_t N, const char** msg);
 // Returns cudaSuccess, or the failing CUDA error; *msg names the failing step.
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg);
 cudaError_t take_status_gemm(unsigned int* out);

@@ -38,7 +38,13 @@ def _unpacked_scales(pa: ops.PackedActivation) -> np.ndarray:
 
 
 def _same_kernel(M):
+    """The unsplit large-M kernel that gemm_packed takes for M rows."""
     return 2 if M <= 128 else 3
+
+
+# the path whose kernels the hand-off of a linear call uses (large-M kernels,
+# split-K included), so its bf16 output must match this path bit for bit
+HAND_OFF_PATH = 4
 
 
 @pytest.mark.parametrize("B,M,N,K,bias", [(1, 300, 512, 1024, True), (1, 64, 256, 512, False),
@@ -52,7 +58,7 @@ def test_hand_off_bytes_equal_the_oracle_quantiser(B, M, N, K, bias):
     x = bf16_to_dev(p.x if B > 1 else p.x[0], dev)
     b = None if p.bias is None else bf16_to_dev(p.bias, dev)
     out, y = ops.linear_quantized_out(x, pw, b)
-    ref = ops.linear(x, pw, b, path=_same_kernel(M))
+    ref = ops.linear(x, pw, b, path=HAND_OFF_PATH)
     ops.check()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), "bf16 output differs from mxfp8_linear"
 
@@ -81,7 +87,7 @@ def test_hand_off_from_prequantised_input():
     xq, xs = ops.quantize(bf16_to_dev(p.x[0], dev))
     b = bf16_to_dev(p.bias, dev)
     out, y = ops.linear_quantized_out(xq, pw, b, x_scale=xs)
-    ref = ops.linear(xq, pw, b, x_scale=xs, path=3)
+    ref = ops.linear(xq, pw, b, x_scale=xs, path=HAND_OFF_PATH)
     ops.check()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     q_ref, s_ref = oracle.quantize(synth.bf16_bits_to_f64(bf16_bits(out))[None])
@@ -106,10 +112,10 @@ def test_three_layer_chain(M):
     out3 = ops.gemm_packed(y2, layers[2][0], biases[2])[0]
     ops.check()
 
-    path = _same_kernel(M)
+    # layer 1 as the hand-off call runs it; layers 2 and 3 as gemm_packed does
     h = x
-    for (pw, _, _), b in zip(layers, biases):
-        h = ops.linear(h, pw, b, path=path)
+    for i, ((pw, _, _), b) in enumerate(zip(layers, biases)):
+        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M))
     ops.check()
     assert torch.equal(out3.view(torch.int16), h.view(torch.int16)), "hand-off chain differs from bf16 chain"
 
