@@ -655,7 +655,8 @@ def _two_layer_chain(ops, dev, flush, stream, pw_up, x, steps):
     return res
 
 
-ONLY = ("prefill_up", "prefill_down", "bmm", "decode_M1", "decode_M16", "decode_M64", "chain_hand_off")
+ONLY = ("prefill_up", "prefill_down", "bmm", "decode_M1", "decode_M16", "decode_M64", "chain_hand_off",
+        "medium_M128", "medium_M256", "medium_M512")
 
 
 def run_only(args):
@@ -670,12 +671,18 @@ def run_only(args):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     w = args.only
-    if w.startswith("decode_M"):
-        M = int(w[len("decode_M"):])
+    if w.startswith("decode_M") or w.startswith("medium_M"):
+        # decode: the first M rows of the decode batch; medium: a prefill chunk
+        # of M bf16 rows on the same N = K = 4096 weights (split K over pairs)
+        M = int(w.split("_M")[1])
         p = synth.decode(64)
         wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
         pw = ops.process_weights(wq, ws)
-        x, bias = _dev_bf16(p.x[0, :M], dev), _dev_bf16(p.bias, dev)
+        bias = _dev_bf16(p.bias, dev)
+        if w.startswith("decode_M"):
+            x = _dev_bf16(p.x[0, :M], dev)
+        else:
+            x = _dev_bf16(synth.to_bf16_bits(synth.normal(77 + M, M * p.K)).reshape(M, p.K), dev)
         out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
         fn = lambda: ops.linear(x, pw, bias, out=out, workspace=wsb)  # noqa: E731

@@ -68,7 +68,8 @@ struct Cfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_OUT = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * STAGE_OUT;
+  static constexpr int OFF_BIAS = OFF_OUT + EPI_WARPS * STAGE_OUT;  // per epilogue warp: its EPI_COLS bias values
+  static constexpr int OFF_BAR = OFF_BIAS + EPI_WARPS * EPI_COLS * 2;
   // per stage: full (operands), sf_full (scale atoms), sf_ready, empty; then acc_full/empty
   static constexpr int NUM_BARS = 4 * STAGES + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -281,11 +282,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int quad = warp & 3;                 // TMEM lane quarter this warp may access
     const int col0 = (ew >> 2) * C::EPI_COLS;
     uint8_t* stage_out = smem + C::OFF_OUT + ew * C::STAGE_OUT;
+    uint4* bias_s = reinterpret_cast<uint4*>(smem + C::OFF_BIAS + ew * C::EPI_COLS * 2);
     uint32_t acc_phase = 0;
     bool pending = false;  // lane 0: a bulk store of this warp may still read stage_out
     for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
       int b, mt, nt;
       tile_coords(tile, args, b, mt, nt);
+      if (args.bias != nullptr) {
+        // this warp's bias values (zero past N) into shared memory while the
+        // tile's MMAs run, so that the drain below reads no global memory
+        if (lane < C::EPI_COLS / 8) {
+          const int n = nt * C::BN + col0 + 8 * lane;
+          bias_s[lane] = n < args.N ? *reinterpret_cast<const uint4*>(args.bias + n) : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
       // accumulator -> registers as bf16 (bias added in fp32, one rounding)
@@ -296,13 +307,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait();
-        const int n0 = nt * C::BN + col0 + c * 32;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float bv[8];
-          const int n = n0 + 8 * g;
-          if (args.bias != nullptr && n < args.N) {
-            const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
+          if (args.bias != nullptr) {
+            const uint4 braw = bias_s[c * 4 + g];
             const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

@@ -70,7 +70,8 @@ constexpr int P_THREADS = 64 + P_SF_WARPS * 32 + P_EPI_THREADS;
 constexpr int P_OFF_A = 0;
 constexpr int P_OFF_B = P_OFF_A + PSTAGES * P_A_BYTES;
 constexpr int P_OFF_OUT = P_OFF_B + PSTAGES * P_B_BYTES;
-constexpr int P_OFF_BAR = P_OFF_OUT + P_EPI_WARPS * P_STAGE_OUT;
+constexpr int P_OFF_BIAS = P_OFF_OUT + P_EPI_WARPS * P_STAGE_OUT;  // per epilogue warp: its 128 bias values
+constexpr int P_OFF_BAR = P_OFF_BIAS + P_EPI_WARPS * P_EPI_COLS * 2;
 // per stage: full (operands of both CTAs, in the even CTA) and empty; per
 // stage pair: sf_ready (in the even CTA); then acc_full, acc_empty
 constexpr int P_NUM_BARS = 2 * PSTAGES + PSTAGES / 2 + 2;
@@ -404,12 +405,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int quad = warp & 3;
     const int col0 = (ew >> 2) * P_EPI_COLS;
     uint8_t* stage_out = smem + P_OFF_OUT + ew * P_STAGE_OUT;
+    uint4* bias_s = reinterpret_cast<uint4*>(smem + P_OFF_BIAS + ew * P_EPI_COLS * 2);
     const uint32_t acc_empty_even = map_shared_rank(smem_u32(acc_empty), 0);
     uint32_t acc_phase = 0;
     bool pending = false;
     for (int u = pair; u < args.units; u += npairs) {
       int b, mt2, nt, sp, kt_lo, kt_hi;
       unit_coords(u, args, b, mt2, nt, sp, kt_lo, kt_hi);
+      if (args.bias != nullptr && args.splits == 1) {
+        // this warp's 128 bias values (zero past N) into shared memory while
+        // the tile's MMAs run, so that the drain below reads no global memory
+        if (lane < P_EPI_COLS / 8) {
+          const int n = nt * PBN + col0 + 8 * lane;
+          bias_s[lane] = n < args.N ? *reinterpret_cast<const uint4*>(args.bias + n) : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
       tc_fence_after();
       const int row0 = mt2 * 2 * PBM + static_cast<int>(rank) * PBM + quad * 32;
@@ -454,13 +465,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait();
-        const int n0 = nt * PBN + col0 + c * 32;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float bv[8];
-          const int n = n0 + 8 * g;
-          if (args.bias != nullptr && n < args.N) {
-            const uint4 braw = *reinterpret_cast<const uint4*>(args.bias + n);
+          if (args.bias != nullptr) {
+            const uint4 braw = bias_s[c * 4 + g];
             const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
