@@ -81,7 +81,10 @@ struct Cfg {
   static constexpr int T_SFB = T_SFA + STAGES * 4;
   static constexpr int T_END = T_SFB + STAGES * NB_ATOMS * 4;
   static constexpr int TMEM_COLS = T_END <= 256 ? 256 : 512;
+  // columns the epilogue's warm-up pass reads (allocated, never written)
+  static constexpr int T_WARM = TMEM_COLS - EPI_COLS;
   static_assert(T_END <= 512, "tensor memory overflow");
+  static_assert(T_WARM >= T_END, "the warm-up columns must be unused");
   static_assert(SMEM_ALLOC <= 232448, "shared memory overflow");
   static_assert(BN % 128 == 0 && BN <= 256, "BN");
   static_assert(EPI_COLS % 32 == 0, "epilogue chunks");
@@ -285,10 +288,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     uint4* bias_s = reinterpret_cast<uint4*>(smem + C::OFF_BIAS + ew * C::EPI_COLS * 2);
     uint32_t acc_phase = 0;
     bool pending = false;  // lane 0: a bulk store of this warp may still read stage_out
-    for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
+    // The first pass (live == false) is a warm-up: it runs the drain and
+    // store code below once, on tensor-memory columns nothing writes, with
+    // every wait, arrive and global write skipped, so that this code is in
+    // the SM's instruction cache when the first accumulator is ready (a
+    // first drain otherwise waits on instruction fetches from DRAM).  The
+    // pass count starts from an opaque register so that one copy of the body
+    // serves both.
+    int pass;
+    asm volatile("mov.s32 %0, -1;" : "=r"(pass));
+    for (int tile = blockIdx.x; tile < args.total_tiles; ++pass) {
+      const bool live = pass >= 0;
       int b, mt, nt;
       tile_coords(tile, args, b, mt, nt);
-      if (args.bias != nullptr) {
+      if (live) tile += gridDim.x;
+      if (live && args.bias != nullptr) {
         // this warp's bias values (zero past N) into shared memory while the
         // tile's MMAs run, so that the drain below reads no global memory
         if (lane < C::EPI_COLS / 8) {
@@ -297,11 +311,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         __syncwarp();
       }
-      if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
-      tc_fence_after();
+      if (live) {
+        if (!mbar_wait(acc_full, acc_phase, abort_flag)) break;
+        tc_fence_after();
+      }
       // accumulator -> registers as bf16 (bias added in fp32, one rounding)
       uint32_t packed[C::EPI_COLS / 2];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::T_ACC + col0;
+      const uint32_t taddr =
+          tmem + (static_cast<uint32_t>(quad * 32) << 16) + (live ? C::T_ACC + col0 : C::T_WARM);
 #pragma unroll
       for (int c = 0; c < C::EPI_COLS / 32; ++c) {
         uint32_t r[32];
@@ -328,13 +345,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                                      __uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);   // accumulator free for the next tile
-      acc_phase ^= 1u;
+      if (live) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);   // accumulator free for the next tile
+        acc_phase ^= 1u;
+      }
 
       // the same bf16 values quantised for the next layer (MXFP8 hand-off)
-      if (args.yq != nullptr)
+      if (live && args.yq != nullptr)
         store_quantized_row128(packed, args.yq, args.ysf, b, mt * BM + quad * 32 + lane, nt * C::BN + col0,
                                args.M, args.N, args.RTY, args.KTY);
       if (!args.store_bf16) continue;
@@ -350,7 +369,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                               packed[c * 16 + 4 * q + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && live) {
           tma_store_3d(&tmOut, stage_out, nt * C::BN + col0 + c * 32, mt * BM + quad * 32, b);
           bulk_commit_group();
           pending = true;
