@@ -181,9 +181,14 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * 256 x 256 output tiles: each tile's K range is split over several pairs,
  * fp32 partials go to the workspace and are added in a fixed order, so the
  * result is the same on every call; this is also what the quantised hand-off
- * uses).  All paths compute the same function; this exists so that tests can
- * check each on every shape.  Path 1 needs M <= 64 and x_bf16 (else
- * MXFP8_ERR_UNSUPPORTED).
+ * uses), 5 = x quantised inside the GEMM (bf16 x read once into shared
+ * memory, quantised there by the same per-block rule into the MMA's operand
+ * tile; no quantised copy of x in memory), one CTA per 128 x 256 output tile
+ * (path 0 never takes it: on B = 16, M = N = 512, K = 7168 it measured no
+ * faster than the quantise kernel plus the CTA-pair GEMM).  All paths compute
+ * the same function; this exists so that tests can check each
+ * on every shape.  Path 1 needs M <= 64 and x_bf16; path 5 needs x_bf16,
+ * N <= 512 and at most one 128 x 256 tile per SM (else MXFP8_ERR_UNSUPPORTED).
  */
 mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
                                const uint8_t* x_scale, int64_t B, int64_t M, int64_t N,

@@ -80,6 +80,23 @@ cudaError_t make_output_map(CUtensorMap* map, void* out, int64_t B, int64_t M, i
 cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, int64_t rows,
                              int64_t K, int box_rows, const char** msg, int fmt = 0);
 
+// gemm_fq.cu: the linear layer with x quantised inside the GEMM (bf16 x
+// [B, M, K] read once, no quantised copy in memory), one CTA per 128 x 256
+// output tile: for shapes whose fused_quantize_tiles(B, M, N) fit on the GPU
+// at once (<= the SM count), N % 8 == 0, K % 128 == 0.
+struct FusedProblem {
+  const void* x;      // bf16 [B, M, K]
+  const uint8_t* w;   // weights [B, N, K] (E4M3, or packed FP6 by wfmt)
+  const uint8_t* sfw; // packed weight scale atoms
+  const void* bias;   // bf16 [N] or nullptr
+  void* out;          // bf16 [B, M, N]
+  int64_t B, M, N, K;
+  int wfmt = 0;
+};
+int64_t fused_quantize_tiles(int64_t B, int64_t M, int64_t N);
+cudaError_t launch_gemm_fq(const FusedProblem& p, int sms, cudaStream_t stream, const char** msg);
+cudaError_t take_status_fq(unsigned int* out);
+
 // gemm_decode.cu: the small-M path (M <= 64, B = 1, bf16 x): weights on the
 // MMA's M side, activations quantised inside the kernel, split-K across a
 // thread-block cluster with a fixed-order reduction in distributed shared memory.

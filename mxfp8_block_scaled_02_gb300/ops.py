@@ -295,8 +295,9 @@ def linear(x: torch.Tensor, pw: PackedWeights, bias: torch.Tensor | None = None,
     given, the pre-quantised E4M3 ``x_q [..., K]`` with row-major scales
     ``[..., K/32]``.  For batched weights (``[B, N, K]``) x is ``[B, M, K]``.
     Returns bf16 ``[..., N]``.  ``path`` forces the small-M (1) or large-M (2)
-    kernel path, or the large-M path on CTA-pair tiles (3); 0 lets the library
-    choose.
+    kernel path, the large-M path on CTA-pair tiles (3), the large-M kernels
+    without the small-M one (4), or the GEMM that quantises bf16 x itself (5);
+    0 lets the library choose.
     """
     quantized = x_scale is not None
     M = _linear_rows(x, pw, bias, x_scale, out)

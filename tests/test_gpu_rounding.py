@@ -147,7 +147,7 @@ def test_fused_quantiser_rounding_is_exact(M):
     xq, xs = oracle.quantize(x)
     exp = _zero_sign_free(synth.to_bf16_bits(oracle.linear(xq, xs, wq, ws)))
     outs = {}
-    for path in (1, 2, 3):                       # fused small-M, one-CTA, CTA-pair
+    for path in (1, 2, 3, 5):                    # fused small-M, one-CTA, CTA-pair, fused large-M
         out = ops.linear(xd, pw, path=path)
         ops.check()
         got = _zero_sign_free(bf16_bits(out))
@@ -159,8 +159,9 @@ def test_fused_quantiser_rounding_is_exact(M):
                 f"{synth.bf16_bits_to_f64(np.array([got[i]]))[0]!r} ref "
                 f"{synth.bf16_bits_to_f64(np.array([exp[i]]))[0]!r}")
         outs[path] = got
-    # the fused quantiser and the standalone one give bit-identical outputs
+    # the fused quantisers and the standalone one give bit-identical outputs
     assert np.array_equal(outs[1], outs[2]) and np.array_equal(outs[2], outs[3])
+    assert np.array_equal(outs[5], outs[2])
     # and the standalone quantiser's codes and scales are the oracle's
     q, s = ops.quantize(xd)
     torch.cuda.synchronize()
