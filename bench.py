@@ -655,8 +655,8 @@ def _two_layer_chain(ops, dev, flush, stream, pw_up, x, steps):
     return res
 
 
-ONLY = ("prefill_up", "prefill_down", "bmm", "decode_M1", "decode_M16", "decode_M64", "chain_hand_off",
-        "medium_M128", "medium_M256", "medium_M512")
+ONLY = ("prefill_up", "prefill_down", "bmm", "bmm_fused", "decode_M1", "decode_M16", "decode_M64",
+        "chain_hand_off", "medium_M128", "medium_M256", "medium_M512")
 
 
 def run_only(args):
@@ -695,13 +695,16 @@ def run_only(args):
         wsb = torch.empty(ops.workspace_size(1, p.M, p.N, p.K, True), dtype=torch.uint8, device=dev)
         fn = lambda: ops.linear(xq, pw, x_scale=xs, out=out, workspace=wsb)  # noqa: E731
     else:
-        p = synth.bmm() if w == "bmm" else synth.prefill_up()
-        x = _dev_bf16(p.x if w == "bmm" else p.x[0], dev)
-        wq, ws = ops.quantize(_dev_bf16(p.w if w == "bmm" else p.w[0], dev))
+        # bmm_fused: the batched workload on the GEMM that quantises x itself (path 5)
+        batched = w.startswith("bmm")
+        p = synth.bmm() if batched else synth.prefill_up()
+        x = _dev_bf16(p.x if batched else p.x[0], dev)
+        wq, ws = ops.quantize(_dev_bf16(p.w if batched else p.w[0], dev))
         pw = ops.process_weights(wq, ws)
         out = torch.empty((*x.shape[:-1], p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(ops.workspace_size(p.B, p.M, p.N, p.K, False), dtype=torch.uint8, device=dev)
-        fn = lambda: ops.linear(x, pw, out=out, workspace=wsb)  # noqa: E731
+        path = 5 if w == "bmm_fused" else 0
+        fn = lambda: ops.linear(x, pw, out=out, workspace=wsb, path=path)  # noqa: E731
         if w == "chain_hand_off":
             r = _two_layer_chain(ops, dev, flush, stream, pw, x, args.steps)
             print(json.dumps({"only": w, **r}), flush=True)
