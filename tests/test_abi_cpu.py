@@ -76,9 +76,10 @@ def test_argument_errors_are_reported_before_launch(lib):
     # misaligned output
     assert lib.mxfp8_linear(fake, None, None, 1, 16, 256, 512, fake, fake, None, P(0x10002), fake,
                             1 << 20, None) == 1
-    # bad path selector
-    assert lib.mxfp8_linear_path(7, fake, None, None, 1, 16, 256, 512, fake, fake, None, fake, fake,
-                                 1 << 20, None) == 1
+    # bad path selector (0..5 are the paths)
+    for bad_path in (-1, 6, 7):
+        assert lib.mxfp8_linear_path(bad_path, fake, None, None, 1, 16, 256, 512, fake, fake, None, fake,
+                                     fake, 1 << 20, None) == 1
     # quantize: K % 32
     assert lib.mxfp8_quantize(fake, 4, 33, fake, fake, None) == 1
     assert lib.mxfp8_quantize(None, 4, 64, fake, fake, None) == 1
