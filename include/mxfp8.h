@@ -277,7 +277,7 @@ mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* 
 /*
  * mxfp8_linear_noalloc - mxfp8_linear for bf16 input, for callers that cannot
  * allocate device memory (no workspace argument).  No counterpart on the
- * paper: the pages' layer always allocates its quantised activation.
+ * source pages: their layer always allocates its quantised activation.
  *   Who needs it: a process whose GPU memory is already owned by another
  *   allocator (a serving runtime that reserves the device at start-up, where a
  *   new cudaMalloc fails or fragments that pool), or a runtime with a fixed
