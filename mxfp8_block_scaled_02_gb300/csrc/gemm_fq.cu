@@ -26,10 +26,14 @@
 //                scale byte into the slot's scale atom; then warps 2..5 (one
 //                per TMEM lane quarter) copy the activation atom and both
 //                weight atoms into the stage's scale columns; afterwards the
-//                same warps drain the accumulator (64 columns each).  The
-//                quantiser is the busiest role: with 8 warps (two blocks per
-//                thread) it took ~0.8 us per K tile, latency-bound at two warps
-//                per scheduler.
+//                same warps drain the accumulator (64 columns each).
+// Measured on that batched shape it is no faster than the quantise kernel
+// followed by the CTA-pair GEMM (63.6 against 63.5 us), which is why the
+// automatic path does not take it: a timing copy whose quantiser skips its
+// loads and conversion still takes ~51 us, so the copy stream of this tiling
+// (128-row boxes of 256 bytes from bf16 rows 14 KB apart, each weight tile
+// read by four CTAs, ~3.6 TB/s) bounds it, not the quantiser (8 or 16
+// quantiser warps measured the same).
 // Every wait is bounded (on expiry the kernel records MXFP8_ERR_TIMEOUT and
 // returns); no named barrier is used, so an expired wait cannot strand a warp.
 #include <cuda_bf16.h>
