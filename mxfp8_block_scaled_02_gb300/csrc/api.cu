@@ -344,22 +344,24 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
     return fail(MXFP8_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   uint8_t* sfa = wsb + ws.sfa_off;
-  const uint8_t* a = x_q;
-  cudaError_t e;
-  if (have_x) {
-    uint8_t* xq = wsb + ws.xq_off;
-    e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s, true);
-    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
-    a = xq;
-  } else {
-    e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s, true);
-    if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
-  }
-  mx::GemmProblem p{a, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K, path == 3 ? 2 : (path == 2 ? 1 : 0),
-                    o.y_q, o.y_sf, w_format};
+  mx::GemmProblem p{have_x ? wsb + ws.xq_off : x_q, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K,
+                    path == 3 ? 2 : (path == 2 ? 1 : 0), o.y_q, o.y_sf, w_format};
   if (splits > 1) {
     p.part = reinterpret_cast<float*>(wsb + ws.part_off);
     p.splits = splits;
+  }
+  cudaError_t e;
+  if (have_x) {
+    e = mx::launch_quantize(x_bf16, B * M, K, wsb + ws.xq_off, sfa, true, B, M, sms, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  } else if (mx::gemm_prefill_uses_pair(p, sms)) {
+    // the CTA-pair kernel's scale writers read the row-major x_scale
+    // themselves: no repack launch
+    p.sfa = x_scale;
+    p.sfa_rowmajor = 1;
+  } else {
+    e = mx::launch_sf_pack(x_scale, B, M, K, sfa, sms, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "activation scale repack launch");
   }
   const char* msg = "";
   e = mx::launch_gemm_prefill(p, sms, s, &msg);

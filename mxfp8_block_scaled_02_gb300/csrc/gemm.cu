@@ -460,11 +460,18 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, i
   return cudaSuccess;
 }
 
-cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
+bool gemm_prefill_uses_pair(const GemmProblem& p, int sms) {
   // 256 x 256 tiles on CTA pairs load 32 KB per SM and K tile against 48 KB
   // for 128 x 256 tiles on one CTA, and measure faster once M spans a pair tile.
-  if (p.tiles == 2 || (p.tiles == 0 && (p.M > 128 || (p.part != nullptr && p.splits > 1)) && sms >= 2))
-    return launch_gemm_pair(p, sms, stream, msg);
+  return p.tiles == 2 || (p.tiles == 0 && (p.M > 128 || (p.part != nullptr && p.splits > 1)) && sms >= 2);
+}
+
+cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {
+  if (gemm_prefill_uses_pair(p, sms)) return launch_gemm_pair(p, sms, stream, msg);
+  if (p.sfa_rowmajor) {
+    *msg = "row-major activation scales need the CTA-pair kernel";
+    return cudaErrorInvalidValue;
+  }
   using C = PrefillCfg;
   static bool attr_set[64] = {};
   int dev = 0;

@@ -92,7 +92,7 @@ static_assert(PSTAGES % 2 == 0, "scale factors are written per pair of stages");
 static_assert(P_EPI_COLS == 128, "the MXFP8 hand-off quantises 128 columns (one scale word) per thread");
 
 struct PArgs {
-  const uint8_t* sfa;
+  const uint8_t* sfa;  // activation scales: packed atoms, or row-major [B, M, K/32] when sfa_rowmajor
   const uint8_t* sfb;
   const __nv_bfloat16* bias;
   uint8_t* yq;   // MXFP8 hand-off outputs (nullptr: none), see mx_epilogue.cuh
@@ -106,6 +106,7 @@ struct PArgs {
   int total_tiles;
   int splits;       // K splits per tile (split-K): > 1 writes fp32 partials through tmPart
   int units;        // total_tiles * splits
+  int sfa_rowmajor; // 1: sfa is the caller's row-major x_scale (no repack kernel before this one)
 };
 
 __device__ __forceinline__ void pair_tile_coords(int tile, const PArgs& a, int& b, int& mt2, int& nt) {
@@ -319,11 +320,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     // Fetch cursor: pointers to this lane's line of the activation atom and
     // of the first weight atom of K tile f_kt of unit f_u; advancing a K
     // tile adds one K-tile row of atoms.
+    // With row-major activation scales the lane gathers its atom line itself:
+    // word i of line `lane` is the 4 scale bytes (blocks 4 kt .. 4 kt + 3) of
+    // tile row lane + 32 i, i.e. 4 aligned bytes of that row (K % 128 == 0);
+    // rows past M read as 0 (their outputs are never stored).
     int f_u = pair, f_kt = 0, f_kt_hi = 0;
     const uint8_t* f_a = nullptr;
     const uint8_t* f_w = nullptr;
     bool f_has_a = false, f_has_w1 = false;
-    const int64_t a_step = static_cast<int64_t>(args.RTA) * kAtomBytes;
+    uint32_t f_rows = 0;  // row-major mode: bit i set when row lane + 32 i is < M
+    const int64_t kb = args.K / 32;
+    const int64_t a_step = args.sfa_rowmajor ? 4 : static_cast<int64_t>(args.RTA) * kAtomBytes;
     const int64_t w_step = static_cast<int64_t>(args.RTB) * kAtomBytes;
     auto start_tile = [&]() {
       if (f_u >= args.units) return;
@@ -333,13 +340,29 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const int64_t arow = static_cast<int64_t>(b) * args.KT + f_kt;
       f_has_a = rt_a < args.RTA;
       f_has_w1 = 2 * nt + 1 < args.RTB;
-      f_a = args.sfa + (arow * args.RTA + (f_has_a ? rt_a : 0)) * kAtomBytes + lane * 16;
+      if (args.sfa_rowmajor) {
+        const int r0 = rt_a * kAtomRows + lane;
+        f_rows = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f_rows |= (r0 + 32 * i < args.M ? 1u : 0u) << i;
+        f_a = args.sfa + (static_cast<int64_t>(b) * args.M + (f_rows & 1u ? r0 : 0)) * kb + 4 * f_kt;
+      } else {
+        f_a = args.sfa + (arow * args.RTA + (f_has_a ? rt_a : 0)) * kAtomBytes + lane * 16;
+      }
       f_w = args.sfb + (arow * args.RTB + 2 * nt) * kAtomBytes + lane * 16;
     };
     start_tile();
     auto fetch = [&](uint4& va, uint4& vb0, uint4& vb1) {
       const uint4 zero = make_uint4(0, 0, 0, 0);
-      va = f_has_a ? __ldg(reinterpret_cast<const uint4*>(f_a)) : zero;
+      if (args.sfa_rowmajor) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[i] = (f_rows >> i) & 1u ? __ldg(reinterpret_cast<const uint32_t*>(f_a + 32 * i * kb)) : 0u;
+        va = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        va = f_has_a ? __ldg(reinterpret_cast<const uint4*>(f_a)) : zero;
+      }
       vb0 = __ldg(reinterpret_cast<const uint4*>(f_w));
       vb1 = f_has_w1 ? __ldg(reinterpret_cast<const uint4*>(f_w + kAtomBytes)) : zero;
       f_a += a_step;
@@ -584,6 +607,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   PArgs a;
   a.sfa = p.sfa;
   a.sfb = p.sfb;
+  a.sfa_rowmajor = p.sfa_rowmajor;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.yq = p.yq;
   a.ysf = p.ysf;

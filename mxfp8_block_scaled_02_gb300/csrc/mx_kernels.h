@@ -53,7 +53,13 @@ struct GemmProblem {
   // ([splits * B][M][N]) and a reduce kernel writes out / the hand-off.
   float* part = nullptr;
   int splits = 1;
+  // 1: sfa is the caller's row-major activation scales [B, M, K/32] instead of
+  // packed atoms (CTA-pair kernel only: its scale writers gather the atom lines)
+  int sfa_rowmajor = 0;
 };
+// Whether launch_gemm_prefill runs p on the CTA-pair kernel (else one CTA per
+// 128 x 256 tile).
+bool gemm_prefill_uses_pair(const GemmProblem& p, int sms);
 // K splits the linear layer uses for a shape (1 = none): enough to give about
 // 64 CTA pairs work when there are at most 16 tiles of 256 x 256, with at least
 // four 128-wide K tiles per split and at most 8 splits.  A function of the

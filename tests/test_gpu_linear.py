@@ -153,6 +153,28 @@ def test_prequantized_equals_bf16_path():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("B,M,N,K,path", [(1, 300, 512, 1024, 3), (3, 200, 264, 512, 3), (2, 130, 136, 384, 0),
+                                          (1, 256, 1024, 2048, 4), (2, 100, 256, 4096, 4)])
+def test_prequantized_scales_read_row_major(B, M, N, K, path):
+    """On the CTA-pair kernel (paths 3, 4 and path 0 above 128 rows; path 4
+    splits K at these shapes) pre-quantised x goes in with its row-major
+    scales, which the kernel's scale writers gather into atom lines
+    themselves; bf16 x goes through the quantise kernel's packed atoms.  Same
+    kernel, same codes and scales: the outputs must be equal bit for bit
+    (ragged rows past M, batches, split-K)."""
+    dev = device()
+    p = synth.make_problem("rowmajor", B, M, N, K, seed=B + M + N, bias_std=0.1)
+    wq, ws = oracle_weights(p)
+    pw = _pack(wq if B > 1 else wq[0], ws if B > 1 else ws[0], dev)
+    x = bf16_to_dev(p.x if B > 1 else p.x[0], dev)
+    bias = bf16_to_dev(p.bias, dev)
+    xq, xs = ops.quantize(x)
+    a = ops.linear(x, pw, bias, path=path)
+    b = ops.linear(xq, pw, bias, x_scale=xs, path=path)
+    ops.check()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_leading_dims_flattened():
     dev = device()
     p = synth.make_problem("lead", 1, 2 * 3 * 5, 128, 256, seed=21)
