@@ -568,6 +568,10 @@ def _other_workloads(ops, dev, flush, stream, steps):
     res["bmm_B16_M512_N512_K7168"] = {
         "us": us, "tflops": p.flops / (us * 1e-6) / 1e12, "gbs": nbytes / (us * 1e-6) / 1e9,
         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm (x bf16 read once)"}
+    # the same layer on the GEMM that quantises x itself (path 5, not the default)
+    us = _time_steps(lambda: ops.linear(x, pw, out=out, workspace=wsb, path=5), flush, stream, steps)
+    res["bmm_B16_M512_N512_K7168_fused_quantize_path5"] = {
+        "us": us, "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm}
     ops.check()
     return res
 
