@@ -660,7 +660,7 @@ def _two_layer_chain(ops, dev, flush, stream, pw_up, x, steps):
 
 
 ONLY = ("prefill_up", "prefill_down", "bmm", "bmm_fused", "decode_M1", "decode_M16", "decode_M64",
-        "chain_hand_off", "medium_M128", "medium_M256", "medium_M512")
+        "chain_hand_off", "medium_M128", "medium_M256", "medium_M512", "up_M128")
 
 
 def run_only(args):
@@ -689,7 +689,7 @@ def run_only(args):
             x = _dev_bf16(synth.to_bf16_bits(synth.normal(77 + M, M * p.K)).reshape(M, p.K), dev)
         out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
-        fn = lambda: ops.linear(x, pw, bias, out=out, workspace=wsb)  # noqa: E731
+        fn = lambda: ops.linear(x, pw, bias, out=out, workspace=wsb, path=args.path)  # noqa: E731
     elif w == "prefill_down":
         p = synth.prefill_down()
         xq, xs = ops.quantize(_dev_bf16(p.x[0], dev))
@@ -697,17 +697,22 @@ def run_only(args):
         pw = ops.process_weights(wq, ws)
         out = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(ops.workspace_size(1, p.M, p.N, p.K, True), dtype=torch.uint8, device=dev)
-        fn = lambda: ops.linear(xq, pw, x_scale=xs, out=out, workspace=wsb)  # noqa: E731
+        fn = lambda: ops.linear(xq, pw, x_scale=xs, out=out, workspace=wsb, path=args.path)  # noqa: E731
     else:
         # bmm_fused: the batched workload on the GEMM that quantises x itself (path 5)
+        # up_M128: a 128-token chunk (the first 128 rows) through the MLP-up
+        # weights: 56 output tiles, so one CTA per 128 x 256 tile, unsplit
         batched = w.startswith("bmm")
         p = synth.bmm() if batched else synth.prefill_up()
         x = _dev_bf16(p.x if batched else p.x[0], dev)
+        if w == "up_M128":
+            x = x[:128].contiguous()
+            p.M = 128
         wq, ws = ops.quantize(_dev_bf16(p.w if batched else p.w[0], dev))
         pw = ops.process_weights(wq, ws)
         out = torch.empty((*x.shape[:-1], p.N), dtype=torch.bfloat16, device=dev)
         wsb = torch.empty(ops.workspace_size(p.B, p.M, p.N, p.K, False), dtype=torch.uint8, device=dev)
-        path = 5 if w == "bmm_fused" else 0
+        path = 5 if w == "bmm_fused" else args.path
         fn = lambda: ops.linear(x, pw, out=out, workspace=wsb, path=path)  # noqa: E731
         if w == "chain_hand_off":
             r = _two_layer_chain(ops, dev, flush, stream, pw, x, args.steps)
@@ -730,6 +735,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=ONLY, default=None,
                     help="time one workload alone (for profiling runs; prints no benchmark line)")
+    ap.add_argument("--path", type=int, default=0, choices=range(6),
+                    help="with --only: the mxfp8_linear_path kernel path (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

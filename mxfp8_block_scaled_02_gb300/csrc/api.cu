@@ -302,7 +302,12 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
 
   // the fused small-M kernel has no quantised-output epilogue: the hand-off
   // always takes the large-M kernels
-  const bool small_ok = have_x && B == 1 && M <= kSmallM && o.y_q == nullptr;
+  // Beyond 32 rows the small-M kernel pays for re-quantising x in every
+  // weight tile's CTAs; it stays faster only while it splits K (measured at
+  // N = 14336, where no split fits: M = 48 took 27.1 us against 22.2 us on
+  // CTA pairs; at N <= 8192, M = 64: 14.4 against 21.2 us).
+  const bool small_ok = have_x && B == 1 && M <= kSmallM && o.y_q == nullptr &&
+                        (path == 1 || M <= 32 || mx::decode_k_splits(M, N, K, sms) >= 2);
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs bf16 x, B == 1 and M <= %d", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {

@@ -463,7 +463,12 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t B, i
 bool gemm_prefill_uses_pair(const GemmProblem& p, int sms) {
   // 256 x 256 tiles on CTA pairs load 32 KB per SM and K tile against 48 KB
   // for 128 x 256 tiles on one CTA, and measure faster once M spans a pair tile.
-  return p.tiles == 2 || (p.tiles == 0 && (p.M > 128 || (p.part != nullptr && p.splits > 1)) && sms >= 2);
+  // Up to 128 rows the layer is bound by streaming the weights: there pairs
+  // are used while one wave of them holds every tile, which puts twice as
+  // many SMs on the stream (3-15 % faster at M = 16..128, N = 4096..14336).
+  const bool one_wave_of_pairs = p.B * ceil_div(p.N, 256) * 2 <= sms;
+  return p.tiles == 2 ||
+         (p.tiles == 0 && (p.M > 128 || one_wave_of_pairs || (p.part != nullptr && p.splits > 1)) && sms >= 2);
 }
 
 cudaError_t launch_gemm_prefill(const GemmProblem& p, int sms, cudaStream_t stream, const char** msg) {

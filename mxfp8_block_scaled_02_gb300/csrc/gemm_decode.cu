@@ -450,6 +450,33 @@ cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStrea
 
 }  // namespace
 
+namespace {
+
+// The largest K split (at most 8, at most one per K tile) whose clusters all
+// fit on the GPU at once, so that every CTA streams its weights from the start.
+template <class C>
+int k_splits(int tiles, int KT, int sms) {
+  int splits = 8;
+  while (splits > 1) {
+    const int fit = max_active_clusters<C>(splits);
+    const bool fits = fit > 0 ? tiles <= fit : tiles * splits <= C::MINB * sms;
+    if (splits <= KT && fits) break;
+    splits >>= 1;
+  }
+  return splits;
+}
+
+}  // namespace
+
+int decode_k_splits(int64_t M, int64_t N, int64_t K, int sms) {
+  const char* msg = "";
+  const int tiles = static_cast<int>(ceil_div(N, kRows));
+  const int KT = static_cast<int>(K / kTK);
+  if (M <= SmallCfg::MAXTOK)
+    return prepare_cfg<SmallCfg>(&msg) == cudaSuccess ? k_splits<SmallCfg>(tiles, KT, sms) : 1;
+  return prepare_cfg<LargeCfg>(&msg) == cudaSuccess ? k_splits<LargeCfg>(tiles, KT, sms) : 1;
+}
+
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg) {
   CUtensorMap mw;
   cudaError_t e = make_operand_map(&mw, p.w, 1, p.N, p.K, kRows, msg, p.wfmt);
@@ -471,16 +498,7 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   const bool small = a.n_mma <= SmallCfg::MAXTOK;
   e = small ? prepare_cfg<SmallCfg>(msg) : prepare_cfg<LargeCfg>(msg);
   if (e != cudaSuccess) return e;
-  // The largest split (at most 8, at most one per K tile) whose clusters all
-  // fit on the GPU at once, so that every CTA streams its weights from the start.
-  const int per_sm = small ? SmallCfg::MINB : LargeCfg::MINB;
-  int splits = 8;
-  while (splits > 1) {
-    const int fit = small ? max_active_clusters<SmallCfg>(splits) : max_active_clusters<LargeCfg>(splits);
-    const bool fits = fit > 0 ? tiles <= fit : tiles * splits <= per_sm * sms;
-    if (splits <= a.KT && fits) break;
-    splits >>= 1;
-  }
+  const int splits = small ? k_splits<SmallCfg>(tiles, a.KT, sms) : k_splits<LargeCfg>(tiles, a.KT, sms);
   a.splits = splits;
   const int grid = tiles * splits;
   return small ? launch_cfg<SmallCfg>(mw, a, grid, stream, msg)

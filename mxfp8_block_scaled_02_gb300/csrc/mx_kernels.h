@@ -116,6 +116,8 @@ struct DecodeProblem {
   int wfmt = 0;      // weight element format, as GemmProblem::wfmt
 };
 constexpr int kDecodeMaxM = 64;
+// The K split (cluster size) launch_gemm_decode uses for this shape; 1 = none.
+int decode_k_splits(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg);
 cudaError_t take_status_decode(unsigned int* out);
 

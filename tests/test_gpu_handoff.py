@@ -37,9 +37,12 @@ def _unpacked_scales(pa: ops.PackedActivation) -> np.ndarray:
     return out.cpu().numpy()
 
 
-def _same_kernel(M):
-    """The unsplit large-M kernel that gemm_packed takes for M rows."""
-    return 2 if M <= 128 else 3
+def _same_kernel(M, B, N):
+    """The unsplit large-M kernel that gemm_packed takes (restated from the
+    library's rule: CTA pairs above 128 rows, or while one wave of pairs holds
+    every 256-column tile; else one CTA per 128 x 256 tile)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 3 if M > 128 or B * -(-N // 256) * 2 <= sms else 2
 
 
 # the path whose kernels the hand-off of a linear call uses (large-M kernels,
@@ -115,7 +118,7 @@ def test_three_layer_chain(M):
     # layer 1 as the hand-off call runs it; layers 2 and 3 as gemm_packed does
     h = x
     for i, ((pw, _, _), b) in enumerate(zip(layers, biases)):
-        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M))
+        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M, 1, pw.N))
     ops.check()
     assert torch.equal(out3.view(torch.int16), h.view(torch.int16)), "hand-off chain differs from bf16 chain"
 

@@ -55,8 +55,12 @@ def _problem(B, M, seed, x_dist="normal"):
     return pw, x, bf16_to_dev(p.bias, dev)
 
 
-def _same_kernel_path(M):
-    return 2 if M <= 128 else 3
+def _same_kernel_path(B, M):
+    """The kernel the no-alloc call runs, as a forced path (restated from the
+    library's rule: CTA pairs above 128 rows, or while one wave of pairs
+    holds every 256-column tile; else one CTA per 128 x 256 tile)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 3 if M > 128 or B * -(-N // 256) * 2 <= sms else 2
 
 
 def _assert_close(got, ref, what):
@@ -77,8 +81,8 @@ def test_noalloc_matches_linear_on_two_calls_in_a_row():
     a1 = _noalloc_abi(x1, pw, bias, 300)     # two calls in a row share the scratch
     a2 = _noalloc_abi(x2, pw, None, 1000)
     ops.check()
-    r1 = ops.linear(x1, pw, bias, path=3)
-    r2 = ops.linear(x2, pw, path=3)
+    r1 = ops.linear(x1, pw, bias, path=_same_kernel_path(1, 300))
+    r2 = ops.linear(x2, pw, path=_same_kernel_path(1, 1000))
     ops.check()
     assert torch.equal(a1[0].view(torch.int16), r1.view(torch.int16))
     assert torch.equal(a2[0].view(torch.int16), r2.view(torch.int16))
@@ -93,7 +97,7 @@ def test_noalloc_binding_equals_linear(B, M):
     pw, x, bias = _problem(B, M, seed=40 + 7 * B + M)
     out = torch.empty((*x.shape[:-1], N), dtype=torch.bfloat16, device=x.device)
     ops.linear_noalloc(x, pw, bias, out=out)
-    same = ops.linear(x, pw, bias, path=_same_kernel_path(M))
+    same = ops.linear(x, pw, bias, path=_same_kernel_path(B, M))
     ops.check()
     assert torch.equal(out.view(torch.int16), same.view(torch.int16)), \
         "noalloc differs from the workspace path on the same kernels"
@@ -102,7 +106,7 @@ def test_noalloc_binding_equals_linear(B, M):
     # a second call on other data into the same output
     x2 = torch.flip(x, dims=[-2]).contiguous()
     ops.linear_noalloc(x2, pw, None, out=out)
-    same2 = ops.linear(x2, pw, None, path=_same_kernel_path(M))
+    same2 = ops.linear(x2, pw, None, path=_same_kernel_path(B, M))
     ops.check()
     assert torch.equal(out.view(torch.int16), same2.view(torch.int16))
 
