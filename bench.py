@@ -405,6 +405,9 @@ def run_ours(args):
     del x_dev, o_dev, x_q, sfa, pa
 
     decode = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 500))
+    # the same kernel on the MLP-up weights (N = 14336, K = 4096, no bias)
+    decode["N14336_K4096"] = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 200), ms=(1, 16),
+                                           problem=synth.prefill_up())
     others = _other_workloads(ops, dev, flush, stream, steps=min(max(n, 10), 100))
     others["two_layer_mlp_M4096"] = _two_layer_chain(ops, dev, flush, stream, pw, x,
                                                      steps=min(max(n, 10), 100))
@@ -461,7 +464,7 @@ def run_ours(args):
     return line
 
 
-def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64)):
+def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64), problem=None):
     """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the layer
     (weights in ``fmt``: E4M3, or packed MXFP6 with 3/4 of the weight bytes).
 
@@ -470,12 +473,14 @@ def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64))
     call reads its weights from HBM), replayed `steps` times; per-call time =
     graph time / R.  Also reported: one call alone after an L2 flush ("cold"),
     which includes the launch and the SM reconfiguration after the flush.
+    ``problem`` replaces the decode weights and x (e.g. the MLP-up weights,
+    N = 14336, taking x from its first rows); its bias may be None.
     """
-    p = synth.decode(64)
+    p = problem if problem is not None else synth.decode(64)
     w = _dev_bf16(p.w[0], dev)
     wq, ws = ops.quantize_weights(w, fmt)
     base = ops.process_weights(wq, ws, fmt)
-    bias = _dev_bf16(p.bias, dev)
+    bias = None if p.bias is None else _dev_bf16(p.bias, dev)
     del w, wq, ws
     per_copy = base.w_packed.numel() + base.sf_packed.numel()
     R = int(np.ceil(2 * 129e6 / per_copy)) + 1
@@ -510,7 +515,8 @@ def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64))
         us = a.elapsed_time(b) * 1e3 / (reps * R)
         cold = _time_steps(lambda: ops.linear(x, base, bias, out=out, workspace=wsb), flush, stream,
                            min(steps, 50))
-        nbytes = base.w_packed.numel() + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N + 2 * p.N
+        nbytes = (base.w_packed.numel() + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N
+                  + (0 if p.bias is None else 2 * p.N))
         res[f"M{M}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
                         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "cold_us": cold,
                         "bytes_per_call": nbytes}
