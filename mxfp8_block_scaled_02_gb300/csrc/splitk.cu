@@ -98,8 +98,11 @@ int splitk_splits(int64_t B, int64_t M, int64_t N, int64_t K) {
   const int64_t kt = K / 128;
   // measured at N = K = 4096 (one call, L2 flushed / in a CUDA graph):
   // 16 tiles split 4 ways 29.4 -> 23.6 / 20.1 -> 16.0 us at M = 128, but
-  // 32 tiles split 2 ways 29.3 -> 31.7 / 21.0 -> 22.2 us at M = 512
-  if (tiles <= 0 || tiles > 16) return 1;
+  // 32 tiles split 2 ways 29.3 -> 31.7 / 21.0 -> 22.2 us at M = 512; with a
+  // long K (>= 64 K tiles) 32 tiles gain from 2 ways: N = 4096, K = 14336
+  // (graph) 50.8 -> 39.8 us at M = 512, 49.4 -> 37.0 at M = 300; K = 8192,
+  // M = 512: 32.4 -> 29.5 us
+  if (tiles <= 0 || tiles > (kt >= 64 ? 32 : 16)) return 1;
   int64_t s = 64 / tiles;
   if (s > kt / 4) s = kt / 4;
   if (s > 8) s = 8;

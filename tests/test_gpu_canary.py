@@ -129,6 +129,7 @@ LINEAR_CASES = [
     (2, 300, 264, 512, 3, "e4m3", True),     # ... gathering row-major scales
     (1, 256, 1032, 2048, 4, "e4m3", False),  # split-K over pairs + reduce
     (2, 100, 264, 4096, 4, "e4m3", True),
+    (1, 300, 4096, 8192, 0, "e4m3", False),  # 32 tiles split two ways (long K)
     (4, 300, 136, 256, 5, "e4m3", False),    # x quantised inside the GEMM
     (1, 5, 264, 512, 1, "e3m2", False),      # MXFP6 weights on each kind of kernel
     (1, 130, 264, 512, 3, "e2m3", False),

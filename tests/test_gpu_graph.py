@@ -42,7 +42,7 @@ def _unpacked_scales(pa):
 def _splits(M, N, K):
     """The split count the library picks for one batch (restated from its rule)."""
     tiles = -(-M // 256) * -(-N // 256)
-    if tiles > 16:
+    if tiles > (32 if K // 128 >= 64 else 16):
         return 1
     s = min(64 // tiles, (K // 128) // 4, 8)
     return s if s >= 2 else 1

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 def splits_for(B, M, N, K):
     """The split count the library uses (restated from its rule)."""
     tiles = B * -(-M // 256) * -(-N // 256)
-    if tiles > 16:
+    if tiles > (32 if K // 128 >= 64 else 16):
         return 1
     s = min(64 // tiles, (K // 128) // 4, 8)
     return s if s >= 2 else 1
@@ -38,6 +38,9 @@ def test_workspace_includes_the_partials():
     base = -(-(B * M * K) // 256) * 256 + -(-ops.packed_sizes(B, M, K)[1] // 256) * 256
     assert ops.workspace_size(B, M, N, K, False) == base + 4 * B * M * N * 4
     assert splits_for(1, 512, 4096, 4096) == 1                      # 32 tiles: not split
+    assert splits_for(1, 512, 4096, 14336) == 2                     # ... unless K is long
+    base = -(-(512 * 14336) // 256) * 256 + -(-ops.packed_sizes(1, 512, 14336)[1] // 256) * 256
+    assert ops.workspace_size(1, 512, 4096, 14336, False) == base + 2 * 512 * 4096 * 4
     assert ops.workspace_size(1, 4096, 14336, 4096, False) == 4096 * 4096 + 32 * 32 * 512   # no split
 
 
@@ -63,7 +66,8 @@ def test_integer_operands_exact(B, M, N, K):
 
 
 @pytest.mark.parametrize("B,M,N,K,bias", [(1, 256, 4096, 4096, True), (1, 200, 1024, 3072, False),
-                                          (3, 130, 264, 2048, True), (1, 65, 4096, 4096, True)])
+                                          (3, 130, 264, 2048, True), (1, 65, 4096, 4096, True),
+                                          (1, 300, 4096, 8192, True)])
 def test_against_oracle_and_deterministic(B, M, N, K, bias):
     dev = device()
     assert splits_for(B, M, N, K) > 1
