@@ -179,3 +179,26 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(ops, "_lib", None)
     with pytest.raises(RuntimeError, match="is missing"):
         ops.load(str(tmp_path / "libmxfp8.so"))
+
+
+def test_workspace_size_follows_the_split_rule(lib):
+    """mxfp8_workspace_size (host only) includes 4 * splits * B * M * N bytes
+    of split-K partials exactly when the shape is split: at most 16 tiles of
+    256 x 256 (at most 32 when K has at least 64 K tiles), min(64 / tiles,
+    K tiles / 4, 8) ways, at least 2."""
+
+    def ws(B, M, N, K, quantized=0):
+        n = ctypes.c_size_t()
+        assert lib.mxfp8_workspace_size(B, M, N, K, quantized, ctypes.byref(n)) == 0
+        return n.value
+
+    def base(B, M, K):
+        a, b = ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.mxfp8_packed_sizes(B, M, K, ctypes.byref(a), ctypes.byref(b)) == 0
+        return -(-(B * M * K) // 256) * 256 + -(-b.value // 256) * 256
+
+    for (B, M, N, K, splits) in [(1, 256, 4096, 4096, 4), (1, 128, 1024, 2048, 4), (1, 512, 4096, 4096, 1),
+                                 (1, 512, 4096, 14336, 2), (1, 300, 4096, 8192, 2), (1, 1024, 4096, 14336, 1),
+                                 (2, 100, 256, 4096, 8), (1, 4096, 14336, 4096, 1)]:
+        parts = 4 * splits * B * M * N if splits > 1 else 0
+        assert ws(B, M, N, K) == base(B, M, K) + parts, (B, M, N, K, splits)
