@@ -34,7 +34,10 @@
 //                (the even CTA's writers first wait for both stages' operands,
 //                so the MMA issuer waits once per two stages);
 //   warps 6..13  epilogue: drain this CTA's accumulator as bf16, arrive on the
-//                even CTA's acc_empty barrier, TMA-store the rows.
+//                even CTA's acc_empty barrier, TMA-store the rows (and, for the
+//                MXFP8 hand-off, their E4M3 codes through the same staging box:
+//                per-row 16-byte stores of the codes measured 4-8 us slower
+//                at MLP-up).
 // One thread issuing every copy of a stage is the first limit here (a TMA or
 // bulk-copy issue costs ~100-150 cycles, a stage of MMAs ~550), which is why
 // the scale atoms do not go through the producer.  Every wait is bounded; a
@@ -141,6 +144,7 @@ __device__ __forceinline__ int64_t pair_steps(int pair, int npairs, const PArgs&
 __global__ void __launch_bounds__(P_THREADS, 1)
     gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPart,
+                          const __grid_constant__ CUtensorMap tmYq,
                           const PArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -174,6 +178,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmOut);
     if (args.splits > 1) prefetch_tmap(&tmPart);
+    if (args.yq != nullptr) prefetch_tmap(&tmYq);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
@@ -536,9 +541,45 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       }
 
       // the same bf16 values quantised for the next layer (MXFP8 hand-off)
-      if (live && args.yq != nullptr)
-        store_quantized_row128(packed, args.yq, args.ysf, b, row0 + lane, nt * PBN + col0, args.M, args.N,
-                               args.RTY, args.KTY);
+      if (args.yq != nullptr) {
+        // the same bf16 values quantised for the next layer: this lane's 128
+        // codes go through the warp's staging box in two 64-column halves
+        // (32 rows x 64 bytes each, TMA stores clip rows past M), the scale
+        // word of its row straight to the packed atoms
+        const int n0 = nt * PBN + col0;
+        uint32_t sword = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 cq[4];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * h + cc;
+            const uint4 v[4] = {make_uint4(packed[16 * c], packed[16 * c + 1], packed[16 * c + 2], packed[16 * c + 3]),
+                                make_uint4(packed[16 * c + 4], packed[16 * c + 5], packed[16 * c + 6], packed[16 * c + 7]),
+                                make_uint4(packed[16 * c + 8], packed[16 * c + 9], packed[16 * c + 10], packed[16 * c + 11]),
+                                make_uint4(packed[16 * c + 12], packed[16 * c + 13], packed[16 * c + 14],
+                                           packed[16 * c + 15])};
+            sword |= quantize_block32(v, cq[2 * cc], cq[2 * cc + 1]) << (8 * c);
+          }
+          if (lane == 0 && pending) bulk_wait_group_read0();
+          __syncwarp();
+          uint4* dst = reinterpret_cast<uint4*>(stage_out + lane * 64);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = cq[q];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && live) {
+            tma_store_3d(&tmYq, stage_out, n0 + 64 * h, row0, b);
+            bulk_commit_group();
+            pending = true;
+          }
+        }
+        const int row = row0 + lane;
+        if (live && row < args.M && n0 < args.N) {
+          const int64_t atom = (static_cast<int64_t>(b) * args.KTY + n0 / kTileK) * args.RTY + (row >> 7);
+          *reinterpret_cast<uint32_t*>(args.ysf + atom * kAtomBytes + (row & 31) * 16 + ((row >> 5) & 3) * 4) = sword;
+        }
+      }
       if (!args.store_bf16) continue;
 #pragma unroll
       for (int c = 0; c < P_EPI_COLS / 32; ++c) {
@@ -586,7 +627,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
     }
     attr_set[dev] = true;
   }
-  CUtensorMap ma, mb, mo, mp;
+  CUtensorMap ma, mb, mo, mp, my;
   cudaError_t e = make_operand_map(&ma, p.a, p.B, p.M, p.K, PBM, msg);
   if (e != cudaSuccess) return e;
   e = make_operand_map(&mb, p.w, p.B, p.N, p.K, PBN / 2, msg, p.wfmt);
@@ -596,6 +637,24 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   // used; any aligned address will do
   void* out_any = p.out != nullptr ? p.out : (p.yq != nullptr ? static_cast<void*>(p.yq) : static_cast<void*>(p.part));
   e = make_output_map(&mo, out_any, p.B, p.M, p.N, msg);
+  if (e != cudaSuccess) return e;
+  if (p.yq != nullptr) {
+    // E4M3 codes [B][M][N], box {64 columns, 32 rows, 1}, no swizzle
+    EncodeTiledFn encode = encode_tiled_fn();
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.B)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M * p.N)};
+    const cuuint32_t box[3] = {64, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode == nullptr ||
+        encode(&my, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p.yq, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS) {
+      *msg = "cuTensorMapEncodeTiled rejected the hand-off codes";
+      return cudaErrorInvalidValue;
+    }
+  } else {
+    my = mo;  // unused
+  }
   if (e != cudaSuccess) return e;
   if (splits > 1) {
     e = make_partial_map(&mp, p.part, static_cast<int64_t>(splits) * p.B, p.M, p.N, msg);
@@ -651,7 +710,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, mp, a);
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf8_pair_kernel, ma, mb, mo, mp, my, a);
   if (e != cudaSuccess) {
     *msg = "pair GEMM launch failed";
     return e;
