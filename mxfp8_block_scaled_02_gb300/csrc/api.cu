@@ -300,12 +300,12 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* out_bf16 = o.out_bf16;
 
-  // the fused small-M kernel has no quantised-output epilogue: the hand-off
-  // always takes the large-M kernels
-  // Beyond 32 rows the small-M kernel pays for re-quantising x in every
-  // weight tile's CTAs; it stays faster only while it splits K (measured at
-  // N = 14336, where no split fits: M = 48 took 27.1 us against 22.2 us on
-  // CTA pairs; at N <= 8192, M = 64: 14.4 against 21.2 us).
+  // The fused small-M kernel has no quantised-output epilogue, so the
+  // hand-off always takes the large-M kernels.  Beyond 32 rows it pays for
+  // re-quantising x in every weight tile's CTAs and stays faster only while
+  // it splits K (measured at N = 14336, where no split fits: M = 48 took
+  // 27.1 us against 22.2 us on CTA pairs; at N <= 8192, M = 64: 14.4 against
+  // 21.2 us).
   const bool small_ok = have_x && B == 1 && M <= kSmallM && o.y_q == nullptr &&
                         (path == 1 || M <= 32 || mx::decode_k_splits(M, N, K, sms) >= 2);
   if (path == 1 && !small_ok)
