@@ -175,10 +175,11 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * (quantisation fused into the GEMM, weights on the MMA's M side), 2 = large-M
  * path with one CTA per 128 x 256 output tile (separate quantise kernel, then
  * the GEMM), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
- * cta_group::2; what path 0 takes for M > 128 when the small-M path does not
- * apply), 4 = the large-M kernels chosen as path 0 chooses them, never the
- * small-M one (CTA pairs with split-K when the shape has at most 16
- * 256 x 256 output tiles: each tile's K range is split over several pairs,
+ * cta_group::2; what path 0 takes when the small-M path does not apply and
+ * M > 128 or one wave of pairs holds every tile, B * ceil(N / 256) <= SMs / 2),
+ * 4 = the large-M kernels chosen as path 0 chooses them, never the small-M one
+ * (CTA pairs with split-K when the shape has at most 16 256 x 256 output
+ * tiles, 32 when K >= 8192: each tile's K range is split over several pairs,
  * fp32 partials go to the workspace and are added in a fixed order, so the
  * result is the same on every call; this is also what the quantised hand-off
  * uses), 5 = x quantised inside the GEMM (bf16 x read once into shared
