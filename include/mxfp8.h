@@ -156,8 +156,10 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
  *   and out are touched only after it has finished.  Of this library's
  *   kernels, only these trigger early: the quantise / activation-scale repack
  *   step inside mxfp8_linear, mxfp8_linear_path and mxfp8_linear_noalloc
- *   (whose output only the same call's GEMM reads, after its wait), and the
- *   small-M GEMM (whose output the next layer reads as x, after its wait).
+ *   (whose output only the same call's GEMM reads, after its wait), the
+ *   CTA-pair GEMM when it splits K (whose partials only the same call's
+ *   reduce reads, after its wait), and the small-M GEMM (whose output the
+ *   next layer reads as x, after its wait).
  *   The standalone calls (mxfp8_quantize, mxfp8_quantize_packed,
  *   mxfp8_pack_scales, mxfp8_process_weights) never do, so weights they write
  *   are complete before a GEMM queued after them starts.  Kernels from other

@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   cluster_sync();  // both CTAs' barriers exist before anyone arrives remotely
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // With split K the next kernel is this call's reduce, which reads the
+  // partials only after its own dependency wait: let it launch now.
+  if (args.splits > 1 && threadIdx.x == 0) launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -38,6 +38,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   const int64_t row = valid ? t / NQ : 0;  // b * M + m
   const int n0 = static_cast<int>(valid ? t - row * NQ : 0) * 8;
   const int64_t base = row * N + n0;
+  // launched with programmatic serialization after the GEMM that writes the
+  // partials: the bias (a weight-side input) is read before the wait, the
+  // partials after it
+  uint4 braw = make_uint4(0, 0, 0, 0);
+  if (valid && bias != nullptr) braw = __ldg(reinterpret_cast<const uint4*>(bias + n0));
+  grid_dependency_wait();
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -65,8 +71,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
       }
     }
     if (bias != nullptr) {
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + n0));
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+      const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[2 * i] += __uint_as_float(bw[i] << 16);
@@ -119,11 +124,18 @@ cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t B, int64
   const int64_t grid = (nq + 255) / 256;
   const int RTY = static_cast<int>(ceil_div(M, kAtomRows)), KTY = static_cast<int>(ceil_div(N, kTileK));
   auto kern = yq != nullptr ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>;
-  kern<<<static_cast<unsigned>(grid), 256, 0, stream>>>(part, splits, B * M * N, nq, static_cast<int>(NQ),
-                                                        static_cast<int>(M), static_cast<int>(N),
-                                                        static_cast<const __nv_bfloat16*>(bias),
-                                                        static_cast<__nv_bfloat16*>(out), yq, ysf, RTY, KTY);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, part, splits, B * M * N, nq, static_cast<int>(NQ), static_cast<int>(M),
+                            static_cast<int>(N), static_cast<const __nv_bfloat16*>(bias),
+                            static_cast<__nv_bfloat16*>(out), yq, ysf, RTY, KTY);
 }
 
 }  // namespace mx
