@@ -349,6 +349,10 @@ def run_ours(args):
                                            flush, stream, k_steps))
     gemm_ms = statistics.mean(_time_calls(lambda: ops.gemm_packed(pa, pw, out=out3), flush, stream,
                                           k_steps))
+    # the floor of this timing method: a kernel that zeroes 256 bytes, timed
+    # the same way (one call between events, L2 flushed before it)
+    tiny = torch.empty(256, dtype=torch.uint8, device=dev)
+    floor_ms = statistics.median(_time_calls(lambda: tiny.zero_(), flush, stream, k_steps))
     ops.check()
 
     peaks, peak_src = _peaks()
@@ -442,6 +446,9 @@ def run_ours(args):
                         "quantize_us": quant_ms * 1e3,
                         "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9,
                         "quantize_hbm_frac": quant_bytes / (quant_ms * 1e-3) / 1e9 / hbm_peak,
+                        "event_floor_us": floor_ms * 1e3,
+                        "event_floor": "a 256-byte zeroing kernel timed the same way: the fixed part of "
+                                       "every per-call time in this block",
                         "gemm_us": gemm_ms * 1e3, "gemm_tflops": gemm_tflops},
             "decode_hbm": decode,
             "other_workloads": others,
@@ -666,7 +673,39 @@ def _two_layer_chain(ops, dev, flush, stream, pw_up, x, steps):
 
 
 ONLY = ("prefill_up", "prefill_down", "bmm", "bmm_fused", "decode_M1", "decode_M16", "decode_M64",
-        "chain_hand_off", "medium_M128", "medium_M256", "medium_M512", "up_M128")
+        "chain_hand_off", "medium_M128", "medium_M256", "medium_M512", "up_M128", "quantize_sweep")
+
+
+def _quantize_sweep(ops, dev, flush, stream, steps):
+    """The quantise step (packed scales, as inside mxfp8_linear) over M at
+    K = 4096, next to a plain device copy of M x K bytes and a kernel that
+    zeroes 256 bytes, all timed the same way (one call between events, L2
+    flushed before it; median of `steps`): separates the per-call floor of the
+    timing method from the kernel's rate.  One JSON line per size."""
+    K = 4096
+    g = torch.Generator(device=dev).manual_seed(11)
+
+    def med(fn):
+        for _ in range(5):
+            fn()
+            flush.zero_()
+        return statistics.median(_time_calls(fn, flush, stream, steps)) * 1e3
+
+    tiny = torch.empty(256, dtype=torch.uint8, device=dev)
+    print(json.dumps({"only": "quantize_sweep", "tiny_kernel_us": med(lambda: tiny.zero_())}), flush=True)
+    for M in (2048, 4096, 8192, 16384):
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        x_q = torch.empty((1, M, K), dtype=torch.uint8, device=dev)
+        sfa = torch.empty(ops.packed_sizes(1, M, K)[1], dtype=torch.uint8, device=dev)
+        src = torch.empty(M * K, dtype=torch.uint8, device=dev)
+        dst = torch.empty(M * K, dtype=torch.uint8, device=dev)
+        q_us = med(lambda: ops.quantize_packed(x, 1, x_q=x_q, sf_packed=sfa))
+        c_us = med(lambda: dst.copy_(src))
+        nbytes = 2 * M * K + M * K + M * K // 32
+        print(json.dumps({"only": "quantize_sweep", "M": M, "K": K, "bytes": nbytes, "quantize_us": q_us,
+                          "copy_MK_bytes_us": c_us}), flush=True)
+        del x, x_q, sfa, src, dst
+    ops.check()
 
 
 def run_only(args):
@@ -681,6 +720,9 @@ def run_only(args):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     w = args.only
+    if w == "quantize_sweep":
+        _quantize_sweep(ops, dev, flush, stream, args.steps)
+        return
     if w.startswith("decode_M") or w.startswith("medium_M"):
         # decode: the first M rows of the decode batch; medium: a prefill chunk
         # of M bf16 rows on the same N = K = 4096 weights (split K over pairs)
