@@ -26,6 +26,7 @@
 //     those rows straight into the owner's receive buffer (remote shared-memory
 //     stores), then one cluster barrier, then each owner sums its S partials
 //     in the fixed order 0..S-1 (deterministic), adds the bias and stores bf16;
+//     with S = 1 the epilogue warps store the output straight from TMEM;
 //   * programmatic dependent launch: the weight loads, which depend on nothing
 //     the previous kernel in the stream writes, start before
 //     griddepcontrol.wait; reading x and writing out come after it, so
@@ -254,8 +255,11 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       }
     }
     {
+      // the column this thread adds the bias to: in the reduction below, or
+      // (one CTA per tile) in the epilogue's direct store, warps 2..5
       const int per = kRows / a.splits;
-      const int n = tile * kRows + static_cast<int>(rank) * per + (threadIdx.x - 64) % per;
+      const int n = a.splits == 1 ? tile * kRows + (warp & 3) * 32 + lane
+                                  : tile * kRows + static_cast<int>(rank) * per + (threadIdx.x - 64) % per;
       if (a.bias != nullptr && n < a.N) bias_n = __bfloat162float(a.bias[n]);
     }
     // x is written by the previous kernel in the stream: wait for it to finish.
@@ -326,8 +330,29 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       if (!quantize_group(g + 1, buf1)) break;
     }
 
-    // ------------------------------------------------ epilogue: TMEM -> owner's receive buffer
-    if (warp < 6 && mbar_wait(acc_full, 0, abort_flag)) {
+    // ------------------------------------------------ epilogue, one CTA per tile: TMEM -> out
+    // (the same sum, in the same order, as the reduction below with S = 1;
+    // measured 14.8 -> 14.1 us per call at M = 1, N = 14336)
+    if (a.splits == 1 && warp < 6 && mbar_wait(acc_full, 0, abort_flag)) {
+      tc_fence_after();
+      const int quad = warp & 3;
+      const int n = tile * kRows + quad * 32 + lane;
+      const uint32_t lrow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      for (int c = 0; c < a.n_mma; c += 16) {
+        uint32_t r[16], r1[16];
+        tmem_ld_32x32b_x16(lrow + C::T_ACC + c, r);
+        tmem_ld_32x32b_x16(lrow + C::T_ACC1 + c, r1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float v = nk > 1 ? __uint_as_float(r[j]) + __uint_as_float(r1[j]) : __uint_as_float(r[j]);
+          if (c + j < a.M && n < a.N)
+            a.out[static_cast<int64_t>(c + j) * a.N + n] = __float2bfloat16_rn((0.f + v) + bias_n);
+        }
+      }
+    }
+    // ------------------------------------------------ epilogue, K split: TMEM -> owner's receive buffer
+    if (a.splits > 1 && warp < 6 && mbar_wait(acc_full, 0, abort_flag)) {
       tc_fence_after();
       const int quad = warp & 3;
       const int wrow = quad * 32 + lane;  // weight row within the tile = TMEM lane
@@ -354,7 +379,7 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
   // ------------------------------------------------ split-K reduction (owner sums)
   tc_fence_before();
   cluster_sync();  // all partials have landed in their owners' receive buffers
-  if (threadIdx.x >= 64 && threadIdx.x < 64 + QTHREADS && !*abort_flag) {
+  if (a.splits > 1 && threadIdx.x >= 64 && threadIdx.x < 64 + QTHREADS && !*abort_flag) {
     const int t = threadIdx.x - 64;
     const int per = kRows / a.splits;
     const float* recv = reinterpret_cast<const float*>(smem + C::OFF_RECV);
