@@ -412,6 +412,9 @@ def run_ours(args):
     # the same kernel on the MLP-up weights (N = 14336, K = 4096, no bias)
     decode["N14336_K4096"] = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 200), ms=(1, 16),
                                            problem=synth.prefill_up())
+    # x handed over already quantised (E4M3 codes + row-major scales)
+    decode["prequantized_x"] = _decode_sweep(ops, dev, flush, stream, steps=min(max(n, 20), 200),
+                                             ms=(1, 16, 64), prequantized=True)
     others = _other_workloads(ops, dev, flush, stream, steps=min(max(n, 10), 100))
     others["two_layer_mlp_M4096"] = _two_layer_chain(ops, dev, flush, stream, pw, x,
                                                      steps=min(max(n, 10), 100))
@@ -471,7 +474,8 @@ def run_ours(args):
     return line
 
 
-def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64), problem=None):
+def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64), problem=None,
+                  prequantized=False):
     """Decode M in {1, 4, 16, 64}, N = K = 4096 with bias: HBM GB/s of the layer
     (weights in ``fmt``: E4M3, or packed MXFP6 with 3/4 of the weight bytes).
 
@@ -482,6 +486,8 @@ def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64),
     which includes the launch and the SM reconfiguration after the flush.
     ``problem`` replaces the decode weights and x (e.g. the MLP-up weights,
     N = 14336, taking x from its first rows); its bias may be None.
+    ``prequantized`` hands the layer x as E4M3 codes and row-major scales
+    (quantised once, before the graph) instead of bf16.
     """
     p = problem if problem is not None else synth.decode(64)
     w = _dev_bf16(p.w[0], dev)
@@ -501,15 +507,19 @@ def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64),
     side = torch.cuda.Stream()
     for M in ms:
         x = _dev_bf16(p.x[0, :M], dev)
+        xs = None
+        if prequantized:
+            x, xs = ops.quantize(x)
         out = torch.empty((M, p.N), dtype=torch.bfloat16, device=dev)
-        wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, False), 1), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(max(ops.workspace_size(1, M, p.N, p.K, prequantized), 1), dtype=torch.uint8,
+                          device=dev)
         for pw in pws:                                   # warm-up outside capture
-            ops.linear(x, pw, bias, out=out, workspace=wsb)
+            ops.linear(x, pw, bias, x_scale=xs, out=out, workspace=wsb)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
             for pw in pws:
-                ops.linear(x, pw, bias, out=out, workspace=wsb)
+                ops.linear(x, pw, bias, x_scale=xs, out=out, workspace=wsb)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
@@ -520,9 +530,10 @@ def _decode_sweep(ops, dev, flush, stream, steps, fmt="e4m3", ms=(1, 4, 16, 64),
         b.record(stream)
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / (reps * R)
-        cold = _time_steps(lambda: ops.linear(x, base, bias, out=out, workspace=wsb), flush, stream,
-                           min(steps, 50))
-        nbytes = (base.w_packed.numel() + p.N * p.K // 32 + 2 * M * p.K + 2 * M * p.N
+        cold = _time_steps(lambda: ops.linear(x, base, bias, x_scale=xs, out=out, workspace=wsb), flush,
+                           stream, min(steps, 50))
+        x_bytes = M * p.K + M * p.K // 32 if prequantized else 2 * M * p.K
+        nbytes = (base.w_packed.numel() + p.N * p.K // 32 + x_bytes + 2 * M * p.N
                   + (0 if p.bias is None else 2 * p.N))
         res[f"M{M}"] = {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9,
                         "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "cold_us": cold,

@@ -174,7 +174,8 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
 /*
  * mxfp8_linear_path - mxfp8_linear with the kernel path chosen by the caller
  * instead of by M: path 0 = automatic (as mxfp8_linear), 1 = small-M path
- * (quantisation fused into the GEMM, weights on the MMA's M side), 2 = large-M
+ * (weights on the MMA's M side; bf16 x quantised inside the GEMM, or a
+ * pre-quantised x_q / x_scale copied into the same operand tiles), 2 = large-M
  * path with one CTA per 128 x 256 output tile (separate quantise kernel, then
  * the GEMM), 3 = large-M path with 256 x 256 tiles on CTA pairs (tcgen05
  * cta_group::2; what path 0 takes when the small-M path does not apply and
@@ -190,7 +191,7 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * (path 0 never takes it: on B = 16, M = N = 512, K = 7168 it measured no
  * faster than the quantise kernel plus the CTA-pair GEMM).  All paths compute
  * the same function; this exists so that tests can check each
- * on every shape.  Path 1 needs M <= 64 and x_bf16; path 5 needs x_bf16,
+ * on every shape.  Path 1 needs B = 1 and M <= 64; path 5 needs x_bf16,
  * N <= 512 and at most one 128 x 256 tile per SM (else MXFP8_ERR_UNSUPPORTED).
  */
 mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,

@@ -306,12 +306,18 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   // it splits K (measured at N = 14336, where no split fits: M = 48 took
   // 27.1 us against 22.2 us on CTA pairs; at N <= 8192, M = 64: 14.4 against
   // 21.2 us).
-  const bool small_ok = have_x && B == 1 && M <= kSmallM && o.y_q == nullptr &&
-                        (path == 1 || M <= 32 || mx::decode_k_splits(M, N, K, sms) >= 2);
+  // A pre-quantised x is copied into the same operand slots instead, with no
+  // re-quantising to pay for: up to 64 rows it is the faster kernel also
+  // where K is not split (N = 14336, K = 4096, graph: M = 48 19.6 against
+  // 21.4 us on CTA pairs, M = 64 19.9 against 21.7 us).
+  const bool small_ok = B == 1 && M <= kSmallM && o.y_q == nullptr &&
+                        (path == 1 || M <= 32 || have_q || mx::decode_k_splits(M, N, K, sms) >= 2);
   if (path == 1 && !small_ok)
-    return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs bf16 x, B == 1 and M <= %d", kSmallM);
+    return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs B == 1, M <= %d and no quantised output", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {
     mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K, w_format};
+    p.xq = x_q;
+    p.xs = x_scale;
     const char* msg = "";
     cudaError_t e = mx::launch_gemm_decode(p, sms, s, &msg);
     if (e != cudaSuccess) return cuda_fail(e, msg);

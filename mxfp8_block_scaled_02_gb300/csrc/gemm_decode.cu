@@ -20,7 +20,9 @@
 //     128-byte-swizzled operand tile and the scales into the scale-factor
 //     atom.  They work on groups of K tiles and issue the next group's loads
 //     before quantising the current one, so the latency of x is paid about
-//     once;
+//     once.  A pre-quantised x (E4M3 codes and row-major scales, the
+//     QuantizedActivation input of apply_weights) takes the same path with the
+//     quantisation replaced by a copy of the block's 32 codes and scale byte;
 //   * the S fp32 partial tiles meet in distributed shared memory: CTA r owns
 //     weight rows [r*128/S, (r+1)*128/S); every CTA stores its partial for
 //     those rows straight into the owner's receive buffer (remote shared-memory
@@ -106,7 +108,9 @@ using SmallCfg = DCfg<16, 8, 8, 1, 1>;
 using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 2, 1>;
 
 struct Args {
-  const uint4* x;  // bf16 [M, K] as 16-byte chunks
+  const uint4* x;  // bf16 [M, K] as 16-byte chunks, or nullptr:
+  const uint8_t* xq;  // pre-quantised E4M3 [M, K] and
+  const uint8_t* xs;  // its row-major scales [M, K/32], copied into the slots
   const uint8_t* sfw;
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
@@ -118,7 +122,10 @@ struct Args {
   int wfmt;    // weight (A operand) element format
 };
 
-template <class C>
+// kPreQ: x arrives pre-quantised (a.xq, a.xs) and is copied, not quantised;
+// a separate instantiation, so that the bf16 path carries no branch for it
+// (a run-time test cost that path ~0.25 us per call at N = K = 4096).
+template <class C, bool kPreQ>
 __global__ void __launch_bounds__(THREADS, C::MINB)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -284,10 +291,18 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         const int i = g * G + ti;
         const int rem = task - ti * per_tile;
         const bool valid = task < per_group && i < nk;
-        const uint4* src =
-            a.x + (static_cast<int64_t>(rem >> 2) * a.K + (kt0 + i) * kTK + (rem & 3) * 32) / 8;
+        const int64_t e0 = static_cast<int64_t>(rem >> 2) * a.K + (kt0 + i) * kTK + (rem & 3) * 32;
+        if (kPreQ) {
+          // pre-quantised: the block's 32 codes and its scale byte
+          const uint4* src = reinterpret_cast<const uint4*>(a.xq + e0);
+          dst[u][0] = valid ? __ldg(src) : make_uint4(0, 0, 0, 0);
+          dst[u][1] = valid ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
+          dst[u][2].x = valid ? static_cast<uint32_t>(__ldg(a.xs + e0 / 32)) : 0u;
+        } else {
+          const uint4* src = a.x + e0 / 8;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) dst[u][k] = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 4; ++k) dst[u][k] = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+        }
       }
     };
     // Wait for the group's ring slots, quantise it into them, signal the MMA.
@@ -303,7 +318,14 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
         const int rem = task - ti * per_tile;
         const int row = rem >> 2, j = rem & 3;
         uint4 c0, c1;
-        const uint32_t sbyte = quantize_block32(cur[u], c0, c1);
+        uint32_t sbyte;
+        if (kPreQ) {
+          c0 = cur[u][0];
+          c1 = cur[u][1];
+          sbyte = cur[u][2].x;
+        } else {
+          sbyte = quantize_block32(cur[u], c0, c1);
+        }
         const int xs = i % C::XSTAGES;
         uint8_t* xrow = smem + C::OFF_X + xs * C::XBYTES + row * 128;
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8);
@@ -409,8 +431,11 @@ cudaError_t prepare_cfg(const char** msg) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<C, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_decode_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_ALLOC);
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
       return e;
@@ -442,7 +467,7 @@ int max_active_clusters(int splits) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<C>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<C, false>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();  // clear the sticky-free error state of the failed query
       n = -1;
     }
@@ -451,7 +476,7 @@ int max_active_clusters(int splits) {
   return cache[dev][slot];
 }
 
-template <class C>
+template <class C, bool kPreQ>
 cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStream_t stream,
                        const char** msg) {
   cudaLaunchConfig_t cfg = {};
@@ -468,7 +493,7 @@ cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStrea
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<C>, mw, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<C, kPreQ>, mw, a);
   if (e != cudaSuccess) *msg = "decode GEMM launch failed";
   return e;
 }
@@ -509,6 +534,8 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
 
   Args a;
   a.x = static_cast<const uint4*>(p.x);
+  a.xq = p.xq;
+  a.xs = p.xs;
   a.sfw = p.sfw;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.out = static_cast<__nv_bfloat16*>(p.out);
@@ -526,8 +553,11 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   const int splits = small ? k_splits<SmallCfg>(tiles, a.KT, sms) : k_splits<LargeCfg>(tiles, a.KT, sms);
   a.splits = splits;
   const int grid = tiles * splits;
-  return small ? launch_cfg<SmallCfg>(mw, a, grid, stream, msg)
-               : launch_cfg<LargeCfg>(mw, a, grid, stream, msg);
+  if (p.xq != nullptr)
+    return small ? launch_cfg<SmallCfg, true>(mw, a, grid, stream, msg)
+                 : launch_cfg<LargeCfg, true>(mw, a, grid, stream, msg);
+  return small ? launch_cfg<SmallCfg, false>(mw, a, grid, stream, msg)
+               : launch_cfg<LargeCfg, false>(mw, a, grid, stream, msg);
 }
 
 cudaError_t take_status_decode(unsigned int* out) {

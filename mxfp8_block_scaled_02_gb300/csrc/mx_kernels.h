@@ -107,13 +107,15 @@ cudaError_t take_status_fq(unsigned int* out);
 // MMA's M side, activations quantised inside the kernel, split-K across a
 // thread-block cluster with a fixed-order reduction in distributed shared memory.
 struct DecodeProblem {
-  const void* x;     // bf16 [M, K]
+  const void* x;     // bf16 [M, K], or nullptr when xq / xs are given
   const uint8_t* w;  // E4M3 [N, K]
   const uint8_t* sfw;
   const void* bias;  // bf16 [N] or nullptr
   void* out;         // bf16 [M, N]
   int64_t M, N, K;
   int wfmt = 0;      // weight element format, as GemmProblem::wfmt
+  const uint8_t* xq = nullptr;  // pre-quantised x: E4M3 [M, K] ...
+  const uint8_t* xs = nullptr;  // ... and its row-major E8M0 scales [M, K/32]
 };
 constexpr int kDecodeMaxM = 64;
 // The K split (cluster size) launch_gemm_decode uses for this shape; 1 = none.

@@ -131,6 +131,8 @@ LINEAR_CASES = [
     (2, 100, 264, 4096, 4, "e4m3", True),
     (1, 300, 4096, 8192, 0, "e4m3", False),  # 32 tiles split two ways (long K)
     (4, 300, 136, 256, 5, "e4m3", False),    # x quantised inside the GEMM
+    (1, 5, 264, 512, 1, "e4m3", True),       # small-M kernel copying a pre-quantised x
+    (1, 40, 520, 1024, 0, "e4m3", True),
     (1, 5, 264, 512, 1, "e3m2", False),      # MXFP6 weights on each kind of kernel
     (1, 130, 264, 512, 3, "e2m3", False),
     (2, 256, 264, 512, 5, "e2m3", False),
