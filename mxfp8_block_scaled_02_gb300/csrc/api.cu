@@ -310,14 +310,37 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   // re-quantising to pay for: up to 64 rows it is the faster kernel also
   // where K is not split (N = 14336, K = 4096, graph: M = 48 19.6 against
   // 21.4 us on CTA pairs, M = 64 19.9 against 21.7 us).
+  // bf16 x beyond 32 rows whose fused CTAs would each re-quantise a long K
+  // range (no split, or K / S > 1024): path 0 quantises x once into the
+  // workspace and the small-M kernel, launched behind the quantiser's early
+  // trigger, copies the codes (graph: N = 14336, K = 4096, M = 48 / 64
+  // 18.3 / 18.5 against 23.0 / 23.2 us on CTA pairs; N = 4096, K = 14336
+  // 18.0 / 19.2 against 22.7 / 23.1 us fused; at N = K = 4096, K / S = 1024,
+  // the fused kernel stays faster: 9.0 / 9.5 against 11.7 / 11.7 us for a
+  // separate quantise call).  Without a workspace of the documented size the
+  // fused kernel runs instead (the same bytes).
+  const int dec_splits = (M > 32 && M <= kSmallM) ? mx::decode_k_splits(M, N, K, sms) : 1;
+  const WsLayout qws = prefill_workspace(1, M, N, K, false, 1);
+  const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && M <= kSmallM && o.y_q == nullptr &&
+                          (dec_splits < 2 || K / dec_splits > 1024) && workspace != nullptr &&
+                          aligned(workspace, 256) && static_cast<int64_t>(workspace_bytes) >= qws.total;
   const bool small_ok = B == 1 && M <= kSmallM && o.y_q == nullptr &&
-                        (path == 1 || M <= 32 || have_q || mx::decode_k_splits(M, N, K, sms) >= 2);
+                        (path == 1 || M <= 32 || have_q || copy_route || dec_splits >= 2);
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs B == 1, M <= %d and no quantised output", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {
     mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K, w_format};
     p.xq = x_q;
     p.xs = x_scale;
+    if (copy_route) {
+      uint8_t* wsb = static_cast<uint8_t*>(workspace);
+      cudaError_t e = mx::launch_quantize(x_bf16, M, K, wsb + qws.xq_off, wsb + qws.sfa_off, false, 1, M, sms, s,
+                                          true);
+      if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+      p.x = nullptr;
+      p.xq = wsb + qws.xq_off;
+      p.xs = wsb + qws.sfa_off;
+    }
     const char* msg = "";
     cudaError_t e = mx::launch_gemm_decode(p, sms, s, &msg);
     if (e != cudaSuccess) return cuda_fail(e, msg);

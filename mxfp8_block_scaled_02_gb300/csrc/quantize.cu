@@ -29,13 +29,19 @@ constexpr int kQU = 2;  // 32-block warp tasks per loop iteration, loads all in 
 // stream start at once (griddepcontrol.launch_dependents): only for the
 // quantise step inside the linear layer, whose GEMM reads the codes and scales
 // after its own dependency wait and loads nothing this kernel writes before it.
+// Those launches are programmatic too: the kernel waits for the one before it
+// (griddepcontrol.wait) before its first read of x or write of anything, so
+// it may be resident early behind a kernel that triggers its dependents.
 // FMT selects the element format (mx_quant.cuh): E4M3, or an FP6 format for
 // MXFP6 weights (row-major scales only).
 template <bool kPacked, bool kEarly, int FMT = kFmtE4M3>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(
     const uint4* __restrict__ x, uint32_t total_blocks, uint32_t KB, uint8_t* __restrict__ q,
     uint8_t* __restrict__ s, uint32_t rows_per_b, uint32_t RT, uint32_t KT) {
-  if (kEarly) launch_dependents();
+  if (kEarly) {
+    launch_dependents();
+    grid_dependency_wait();
+  }
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -181,10 +187,18 @@ cudaError_t launch_quantize_t(const void* x, int64_t total_blocks, int64_t K, ui
   const int grid = grid_for(ceil_div(ntasks, kQU) * 32, kQuantThreads, sms, per_sm);
   const uint32_t RT = static_cast<uint32_t>(ceil_div(rows_per_b, kAtomRows));
   const uint32_t KT = static_cast<uint32_t>(ceil_div(K, kTileK));
-  quantize_kernel<kPacked, kEarly, FMT><<<grid, kQuantThreads, 0, stream>>>(
-      static_cast<const uint4*>(x), static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(K / 32), q, s,
-      static_cast<uint32_t>(rows_per_b), RT, KT);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kQuantThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kEarly ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<kPacked, kEarly, FMT>, static_cast<const uint4*>(x),
+                            static_cast<uint32_t>(total_blocks), static_cast<uint32_t>(K / 32), q, s,
+                            static_cast<uint32_t>(rows_per_b), RT, KT);
 }
 
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,

@@ -72,3 +72,21 @@ def test_arbitrary_codes_match_oracle(M, N, K):
     ops.check()
     assert_close(y1, ref, f"small-M, M={M} N={N} K={K}")
     assert_close(y2, ref, f"one-CTA tiles, M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(40, 264, 9216), (64, 1032, 16384), (33, 10240, 1024), (48, 4096, 4096)])
+def test_bf16_rows_33_to_64_route(M, N, K):
+    """Beyond 32 rows path 0 may quantise x once into the workspace and run the
+    small-M kernel on the codes (when its CTAs would each re-quantise a long K
+    range): the bytes are those of the fused small-M kernel (path 1)."""
+    dev = device()
+    w = _bf16((N, K), N + K, dev, 0.05)
+    wq, ws = ops.quantize(w)
+    pw = ops.process_weights(wq, ws)
+    x = _bf16((M, K), M, dev)
+    b = _bf16((N,), K, dev, 0.1)
+    y0 = ops.linear(x, pw, b)
+    y1 = ops.linear(x, pw, b, path=1)
+    torch.cuda.synchronize()
+    ops.check()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
