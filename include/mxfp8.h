@@ -288,9 +288,12 @@ mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* 
  *   memory plan that forbids allocation after initialisation.
  *   Scratch: a file-scope device array of MXFP8_NOALLOC_SCRATCH_BYTES (32 MiB)
  *   inside the library, held by every GPU that loads the library until the
- *   process exits.  The call needs round_up(B*M*K, 256) + round_up(packed
- *   scale bytes of (B, M, K), 256) bytes of it and returns
- *   MXFP8_ERR_UNSUPPORTED beyond that (e.g. M*K above ~32.5 M at B = 1).
+ *   process exits.  With B = 1 and M <= 32 (or M <= 64 where the small-M
+ *   kernel splits K, as mxfp8_linear decides) the call runs the small-M
+ *   kernel, which quantises x inside the GEMM and uses no scratch; otherwise it needs
+ *   round_up(B*M*K, 256) + round_up(packed scale bytes of (B, M, K), 256)
+ *   bytes of it and returns MXFP8_ERR_UNSUPPORTED beyond that (e.g. M*K above
+ *   ~32.5 M at B = 1).
  *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call

@@ -91,20 +91,30 @@ extern "C" mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int6
   if (!aligned(x_bf16, 16) || !aligned(w_packed, 16) || !aligned(sf_packed, 16) ||
       !aligned(out_bf16, 16) || (bias_bf16 != nullptr && !aligned(bias_bf16, 16)))
     return fail(MXFP8_ERR_INVALID_ARG, "mxfp8_linear_noalloc: pointers must be 16-byte aligned");
+  uint8_t* scratch = nullptr;
+  int sms = 0;
+  mxfp8_status st = scratch_for_current_device(&scratch, &sms);
+  if (st != MXFP8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (B == 1 && M <= mx::kDecodeMaxM && (M <= 32 || mx::decode_k_splits(M, N, K, sms) >= 2)) {
+    // the small-M kernel quantises x inside the GEMM and needs no scratch
+    // (mxfp8_linear's automatic path takes it for bf16 x at these sizes)
+    mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K};
+    const char* msg = "";
+    e = mx::launch_gemm_decode(p, sms, s, &msg);
+    if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "mxfp8_linear_noalloc: small-M GEMM launch failed");
+    return MXFP8_OK;
+  }
   const int64_t xq_bytes = round_up(B * M * K, 256);
   const int64_t sfa_bytes = round_up(mx::sf_packed_bytes(B, M, K), 256);
   if (xq_bytes + sfa_bytes > kNoallocScratchBytes)
     return fail(MXFP8_ERR_UNSUPPORTED,
                 "mxfp8_linear_noalloc: B*M*K plus the packed scales exceeds the fixed scratch "
                 "(MXFP8_NOALLOC_SCRATCH_BYTES); use mxfp8_linear with a workspace");
-  uint8_t* scratch = nullptr;
-  int sms = 0;
-  mxfp8_status st = scratch_for_current_device(&scratch, &sms);
-  if (st != MXFP8_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* xq = scratch;
   uint8_t* sfa = scratch + xq_bytes;
-  cudaError_t e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s, true);
+  e = mx::launch_quantize(x_bf16, B * M, K, xq, sfa, true, B, M, sms, s, true);
   if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "mxfp8_linear_noalloc: quantize launch failed");
   mx::GemmProblem p{xq, w_packed, sfa, sf_packed, bias_bf16, out_bf16, B, M, N, K};
   const char* msg = "";
