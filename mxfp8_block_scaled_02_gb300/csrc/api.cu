@@ -300,25 +300,20 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* out_bf16 = o.out_bf16;
 
-  // The fused small-M kernel has no quantised-output epilogue, so the
-  // hand-off always takes the large-M kernels.  Beyond 32 rows it pays for
-  // re-quantising x in every weight tile's CTAs and stays faster only while
-  // it splits K (measured at N = 14336, where no split fits: M = 48 took
-  // 27.1 us against 22.2 us on CTA pairs; at N <= 8192, M = 64: 14.4 against
-  // 21.2 us).
-  // A pre-quantised x is copied into the same operand slots instead, with no
-  // re-quantising to pay for: up to 64 rows it is the faster kernel also
-  // where K is not split (N = 14336, K = 4096, graph: M = 48 19.6 against
-  // 21.4 us on CTA pairs, M = 64 19.9 against 21.7 us).
-  // bf16 x beyond 32 rows whose fused CTAs would each re-quantise a long K
-  // range (no split, or K / S > 1024): path 0 quantises x once into the
-  // workspace and the small-M kernel, launched behind the quantiser's early
-  // trigger, copies the codes (graph: N = 14336, K = 4096, M = 48 / 64
-  // 18.3 / 18.5 against 23.0 / 23.2 us on CTA pairs; N = 4096, K = 14336
-  // 18.0 / 19.2 against 22.7 / 23.1 us fused; at N = K = 4096, K / S = 1024,
-  // the fused kernel stays faster: 9.0 / 9.5 against 11.7 / 11.7 us for a
-  // separate quantise call).  Without a workspace of the documented size the
-  // fused kernel runs instead (the same bytes).
+  // The small-M kernel (every threshold below measured in CUDA graphs of
+  // back-to-back calls):
+  //  * has no quantised-output epilogue: the hand-off takes the large-M kernels;
+  //  * up to 32 rows, quantises bf16 x inside every CTA;
+  //  * from 33 to 64 rows of bf16 x, does so only while each CTA's K range is
+  //    short (K split, K / S <= 1024: N = K = 4096, M = 48 / 64 9.0 / 9.5 us);
+  //    otherwise path 0 quantises x once into the workspace and the kernel,
+  //    launched behind the quantiser's early trigger, copies the codes
+  //    (N = 14336, K = 4096: 18.3 / 18.5 us against 23.0 / 23.2 on CTA pairs
+  //    and 25.1 / 25.0 re-quantising in every CTA; N = 4096, K = 14336:
+  //    18.0 / 19.2 against 22.7 / 23.1 us re-quantising); with a workspace
+  //    below the documented size it re-quantises instead (the same bytes);
+  //  * copies a pre-quantised x, up to 64 rows (N = 14336, M = 48 / 64:
+  //    19.6 / 19.9 us against 21.4 / 21.7 on CTA pairs).
   const int dec_splits = (M > 32 && M <= kSmallM) ? mx::decode_k_splits(M, N, K, sms) : 1;
   const WsLayout qws = prefill_workspace(1, M, N, K, false, 1);
   const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && M <= kSmallM && o.y_q == nullptr &&
