@@ -602,8 +602,9 @@ def _other_workloads(ops, dev, flush, stream, steps):
 
 def _medium_m(ops, dev, flush, stream, steps):
     """Prefill chunks of 128 / 256 / 512 tokens at N = K = 4096 (bf16 x, one
-    call after an L2 flush): few output tiles, so the library splits K over CTA
-    pairs; the unsplit CTA-pair path (path 3) beside it."""
+    call after an L2 flush): the library's choice (path 0: the small-M kernel
+    at 128 rows, split K over CTA pairs at 256), split-K CTA pairs (path 4)
+    and unsplit CTA pairs (path 3)."""
     p = synth.decode(64)       # N = K = 4096 weights and bias of the decode workload
     wq, ws = ops.quantize(_dev_bf16(p.w[0], dev))
     pw = ops.process_weights(wq, ws)
@@ -615,7 +616,7 @@ def _medium_m(ops, dev, flush, stream, steps):
         wsb = torch.empty(ops.workspace_size(1, M, p.N, p.K, False), dtype=torch.uint8, device=dev)
         flops = 2.0 * M * p.N * p.K
         r = {}
-        for name, path in (("split_k", 0), ("unsplit_pairs", 3)):
+        for name, path in (("automatic", 0), ("split_k", 4), ("unsplit_pairs", 3)):
             us = _time_steps(lambda: ops.linear(x, pw, bias, out=out, workspace=wsb, path=path), flush, stream,
                              steps)
             r[name] = {"us": us, "tflops": flops / (us * 1e-6) / 1e12}

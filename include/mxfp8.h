@@ -191,7 +191,7 @@ mxfp8_status mxfp8_linear(const void* x_bf16, const uint8_t* x_q, const uint8_t*
  * (path 0 never takes it: on B = 16, M = N = 512, K = 7168 it measured no
  * faster than the quantise kernel plus the CTA-pair GEMM).  All paths compute
  * the same function; this exists so that tests can check each
- * on every shape.  Path 1 needs B = 1 and M <= 64; path 5 needs x_bf16,
+ * on every shape.  Path 1 needs B = 1 and M <= 128; path 5 needs x_bf16,
  * N <= 512 and at most one 128 x 256 tile per SM (else MXFP8_ERR_UNSUPPORTED).
  */
 mxfp8_status mxfp8_linear_path(int path, const void* x_bf16, const uint8_t* x_q,
@@ -289,8 +289,9 @@ mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* 
  *   Scratch: a file-scope device array of MXFP8_NOALLOC_SCRATCH_BYTES (32 MiB)
  *   inside the library, held by every GPU that loads the library until the
  *   process exits.  With B = 1 and M <= 32 (or M <= 64 where the small-M
- *   kernel splits K, as mxfp8_linear decides) the call runs the small-M
- *   kernel, which quantises x inside the GEMM and uses no scratch; otherwise it needs
+ *   kernel splits K, or M <= 128 where it splits K into ranges of at most
+ *   1024) the call runs the small-M kernel, which quantises x inside the
+ *   GEMM and uses no scratch; otherwise it needs
  *   round_up(B*M*K, 256) + round_up(packed scale bytes of (B, M, K), 256)
  *   bytes of it and returns MXFP8_ERR_UNSUPPORTED beyond that (e.g. M*K above
  *   ~32.5 M at B = 1).

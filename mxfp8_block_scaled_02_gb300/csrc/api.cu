@@ -73,7 +73,7 @@ mxfp8_status current_device(int* sms) {
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kSmallM = mx::kDecodeMaxM;  // largest M the fused small-M path serves
+constexpr int kSmallM = mx::kDecodeMaxM;  // largest M the small-M kernel takes
 
 struct WsLayout {
   int64_t xq_off, xq_bytes, sfa_off, sfa_bytes, part_off, part_bytes, total;
@@ -313,14 +313,23 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   //    18.0 / 19.2 against 22.7 / 23.1 us re-quantising); with a workspace
   //    below the documented size it re-quantises instead (the same bytes);
   //  * copies a pre-quantised x, up to 64 rows (N = 14336, M = 48 / 64:
-  //    19.6 / 19.9 us against 21.4 / 21.7 on CTA pairs).
+  //    19.6 / 19.9 us against 21.4 / 21.7 on CTA pairs);
+  //  * from 65 to 128 rows (its 128-token shape), serves only where the K
+  //    split leaves each CTA a short K range (K / S <= 1024), bf16 x
+  //    quantised once and copied: N = K = 4096, M = 65 / 96 / 128
+  //    12.0 / 12.6 / 14.1 us (pre-quantised 9.8 / 10.4 / 10.8) against
+  //    15.4 / 16.1 / 16.4 (15.0 / 15.8 / 16.4) on split-K CTA pairs; with
+  //    longer K ranges (N = 14336 unsplit, or K = 14336) it took 27-33 us
+  //    against 22-25 and the CTA pairs stay.
   const int dec_splits = (M > 32 && M <= kSmallM) ? mx::decode_k_splits(M, N, K, sms) : 1;
+  const bool short_k = dec_splits >= 2 && K / dec_splits <= 1024;  // each CTA's K range
+  const bool wide_ok = M > 64 && M <= kSmallM && short_k;
   const WsLayout qws = prefill_workspace(1, M, N, K, false, 1);
-  const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && M <= kSmallM && o.y_q == nullptr &&
-                          (dec_splits < 2 || K / dec_splits > 1024) && workspace != nullptr &&
-                          aligned(workspace, 256) && static_cast<int64_t>(workspace_bytes) >= qws.total;
+  const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && o.y_q == nullptr &&
+                          ((M <= 64 && !short_k) || wide_ok) && workspace != nullptr && aligned(workspace, 256) &&
+                          static_cast<int64_t>(workspace_bytes) >= qws.total;
   const bool small_ok = B == 1 && M <= kSmallM && o.y_q == nullptr &&
-                        (path == 1 || M <= 32 || have_q || copy_route || dec_splits >= 2);
+                        (path == 1 || M <= 32 || (M <= 64 && (have_q || copy_route || dec_splits >= 2)) || wide_ok);
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs B == 1, M <= %d and no quantised output", kSmallM);
   if (path == 1 || (path == 0 && small_ok)) {

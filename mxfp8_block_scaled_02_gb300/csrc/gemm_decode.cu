@@ -1,13 +1,13 @@
 // gemm_decode.cu - the small-M (decode) path of the MXFP8 linear layer.
 //
-// out[m, n] = bf16( sum_k deq(x)[m, k] * deq(w)[n, k] + bias[n] ), M <= 64,
+// out[m, n] = bf16( sum_k deq(x)[m, k] * deq(w)[n, k] + bias[n] ), M <= 128,
 // with x bf16 quantised to MXFP8 inside the kernel: the block-scaled product
 // and bias add of "AiterFlyDSLMxfp8LinearKernel.apply_weights" (aiter_flydsl
 // page), with its mxfp8_e4m3_quantize step fused into the GEMM producer.
 //
 // At small M the layer is bound by reading the weights once from HBM, so:
 //   * the weights are the MMA's A operand (M = 128 weight rows per CTA) and the
-//     tokens its B operand (N = 16, 32 or 64 >= M), so no MMA rows are wasted
+//     tokens its B operand (N = 16, 32, 64 or 128 >= M), so no MMA rows are wasted
 //     on padding tokens;
 //   * K is split over a cluster of S CTAs (S in {1, 2, 4, 8}, the largest
 //     whose clusters all fit on the GPU at once); each CTA streams its
@@ -37,8 +37,9 @@
 //     shared slots, quantising the second half of a CTA's K slice had to wait
 //     for the MMAs of the first half, a round trip on every call's critical
 //     path (dependency wait -> x -> MMAs -> reduction).
-// Two shapes of the kernel: up to 16 tokens (8-stage weight ring, ~165 KB of
-// shared memory) and up to 64 tokens (6-stage weight ring), one CTA per SM.
+// Three shapes of the kernel: up to 16 tokens (8-stage weight ring, ~165 KB of
+// shared memory), up to 64 tokens (6-stage weight ring) and up to 128 tokens
+// (4-slot weight and activation rings, 512 TMEM columns), one CTA per SM.
 // Warp roles: 0 = TMA producer (weights + weight scales), 1 = TMEM allocator
 // and MMA issuer for the even K tiles, 10 = MMA issuer for the odd K tiles
 // (each into its own accumulator; issuing a K tile's copies and MMAs takes one
@@ -92,8 +93,9 @@ struct DCfg {
   static constexpr int T_SFW = 2 * MAXTOK;
   static constexpr int T_SFX = T_SFW + 4 * STAGES;
   static constexpr int T_END = T_SFX + 4 * STAGES;
-  static constexpr int TMEM_COLS = T_END <= 32 ? 32 : (T_END <= 64 ? 64 : (T_END <= 128 ? 128 : 256));
-  static_assert(T_END <= 256, "tensor memory");
+  static constexpr int TMEM_COLS =
+      T_END <= 32 ? 32 : (T_END <= 64 ? 64 : (T_END <= 128 ? 128 : (T_END <= 256 ? 256 : 512)));
+  static_assert(T_END <= 512, "tensor memory");
   static_assert(MINB * SMEM_ALLOC <= 232448, "shared memory");
   static_assert(QTHREADS % kRows == 0, "each reduction thread owns one output column");
 };
@@ -105,7 +107,10 @@ struct DCfg {
 // measured 8.45 us per call at M = 1 against 9.10 us for a 4-stage ring at two
 // CTAs per SM, whose second half of the slice refilled on the critical path.
 using SmallCfg = DCfg<16, 8, 8, 1, 1>;
-using LargeCfg = DCfg<kDecodeMaxM, 6, 8, 2, 1>;
+using LargeCfg = DCfg<64, 6, 8, 2, 1>;
+// Up to 128 tokens (a prefill chunk): 4-slot rings of 16 KB weight tiles and
+// 16 KB code tiles, a 64 KB receive buffer, two 128-column accumulators.
+using WideCfg = DCfg<kDecodeMaxM, 4, 4, 2, 1>;
 
 struct Args {
   const uint4* x;  // bf16 [M, K] as 16-byte chunks, or nullptr:
@@ -524,8 +529,24 @@ int decode_k_splits(int64_t M, int64_t N, int64_t K, int sms) {
   const int KT = static_cast<int>(K / kTK);
   if (M <= SmallCfg::MAXTOK)
     return prepare_cfg<SmallCfg>(&msg) == cudaSuccess ? k_splits<SmallCfg>(tiles, KT, sms) : 1;
-  return prepare_cfg<LargeCfg>(&msg) == cudaSuccess ? k_splits<LargeCfg>(tiles, KT, sms) : 1;
+  if (M <= LargeCfg::MAXTOK)
+    return prepare_cfg<LargeCfg>(&msg) == cudaSuccess ? k_splits<LargeCfg>(tiles, KT, sms) : 1;
+  return prepare_cfg<WideCfg>(&msg) == cudaSuccess ? k_splits<WideCfg>(tiles, KT, sms) : 1;
 }
+
+namespace {
+
+template <class C>
+cudaError_t launch_with(const CUtensorMap& mw, Args& a, bool preq, int sms, cudaStream_t stream,
+                        const char** msg) {
+  cudaError_t e = prepare_cfg<C>(msg);
+  if (e != cudaSuccess) return e;
+  a.splits = k_splits<C>(a.RTW, a.KT, sms);
+  const int grid = a.RTW * a.splits;
+  return preq ? launch_cfg<C, true>(mw, a, grid, stream, msg) : launch_cfg<C, false>(mw, a, grid, stream, msg);
+}
+
+}  // namespace
 
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg) {
   CUtensorMap mw;
@@ -543,21 +564,14 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   a.N = static_cast<int>(p.N);
   a.K = static_cast<int>(p.K);
   a.wfmt = p.wfmt;
-  a.n_mma = p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64);  // a power of two: shifts in the quantiser
+  // MMA N: a power of two (shifts in the quantiser), at least M
+  a.n_mma = p.M <= 16 ? 16 : (p.M <= 32 ? 32 : (p.M <= 64 ? 64 : 128));
   a.KT = static_cast<int>(p.K / kTK);
   a.RTW = static_cast<int>(ceil_div(p.N, kAtomRows));
-  const int tiles = a.RTW;
-  const bool small = a.n_mma <= SmallCfg::MAXTOK;
-  e = small ? prepare_cfg<SmallCfg>(msg) : prepare_cfg<LargeCfg>(msg);
-  if (e != cudaSuccess) return e;
-  const int splits = small ? k_splits<SmallCfg>(tiles, a.KT, sms) : k_splits<LargeCfg>(tiles, a.KT, sms);
-  a.splits = splits;
-  const int grid = tiles * splits;
-  if (p.xq != nullptr)
-    return small ? launch_cfg<SmallCfg, true>(mw, a, grid, stream, msg)
-                 : launch_cfg<LargeCfg, true>(mw, a, grid, stream, msg);
-  return small ? launch_cfg<SmallCfg, false>(mw, a, grid, stream, msg)
-               : launch_cfg<LargeCfg, false>(mw, a, grid, stream, msg);
+  const bool preq = p.xq != nullptr;
+  if (a.n_mma <= SmallCfg::MAXTOK) return launch_with<SmallCfg>(mw, a, preq, sms, stream, msg);
+  if (a.n_mma <= LargeCfg::MAXTOK) return launch_with<LargeCfg>(mw, a, preq, sms, stream, msg);
+  return launch_with<WideCfg>(mw, a, preq, sms, stream, msg);
 }
 
 cudaError_t take_status_decode(unsigned int* out) {

@@ -117,7 +117,7 @@ struct DecodeProblem {
   const uint8_t* xq = nullptr;  // pre-quantised x: E4M3 [M, K] ...
   const uint8_t* xs = nullptr;  // ... and its row-major E8M0 scales [M, K/32]
 };
-constexpr int kDecodeMaxM = 64;
+constexpr int kDecodeMaxM = 128;  // largest M the small-M kernel takes
 // The K split (cluster size) launch_gemm_decode uses for this shape; 1 = none.
 int decode_k_splits(int64_t M, int64_t N, int64_t K, int sms);
 cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t stream, const char** msg);

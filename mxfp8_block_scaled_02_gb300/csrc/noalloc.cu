@@ -97,9 +97,11 @@ extern "C" mxfp8_status mxfp8_linear_noalloc(const void* x_bf16, int64_t B, int6
   if (st != MXFP8_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (B == 1 && M <= mx::kDecodeMaxM && (M <= 32 || mx::decode_k_splits(M, N, K, sms) >= 2)) {
+  const int dec_splits = (B == 1 && M > 32 && M <= mx::kDecodeMaxM) ? mx::decode_k_splits(M, N, K, sms) : 1;
+  if (B == 1 && (M <= 32 || (M <= 64 && dec_splits >= 2) ||
+                 (M <= mx::kDecodeMaxM && dec_splits >= 2 && K / dec_splits <= 1024))) {
     // the small-M kernel quantises x inside the GEMM and needs no scratch
-    // (mxfp8_linear's automatic path takes it for bf16 x at these sizes)
+    // (the shapes mxfp8_linear's automatic path gives it)
     mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K};
     const char* msg = "";
     e = mx::launch_gemm_decode(p, sms, s, &msg);

@@ -28,7 +28,8 @@ def _bf16(shape, seed, dev, scale=1.0):
 @pytest.mark.parametrize("M,N,K,fmt,bias", [(1, 4096, 4096, "e4m3", True), (5, 264, 512, "e4m3", False),
                                             (16, 4096, 4096, "e4m3", True), (33, 1032, 2048, "e4m3", True),
                                             (64, 4096, 4096, "e4m3", False), (1, 14336, 4096, "e4m3", True),
-                                            (7, 264, 1024, "e2m3", True), (16, 520, 512, "e3m2", False)])
+                                            (7, 264, 1024, "e2m3", True), (16, 520, 512, "e3m2", False),
+                                            (100, 1032, 2048, "e4m3", True), (128, 4096, 4096, "e4m3", False)])
 def test_same_bytes_as_bf16_input(M, N, K, fmt, bias):
     """x_q, x_scale = quantize(x): the small-M kernel gives bit for bit what it
     gives on x itself, and path 0 routes both forms to kernels that agree."""
@@ -49,7 +50,8 @@ def test_same_bytes_as_bf16_input(M, N, K, fmt, bias):
     assert torch.equal(y_auto_bf.view(torch.int16), y_auto_q.view(torch.int16)), "path 0: the two forms differ"
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 264, 512), (9, 1032, 1024), (64, 264, 256), (16, 4096, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1, 264, 512), (9, 1032, 1024), (64, 264, 256), (16, 4096, 4096),
+                                   (128, 264, 1024), (97, 520, 4096)])
 def test_arbitrary_codes_match_oracle(M, N, K):
     """Codes and scales that no quantiser produced (every finite E4M3 code,
     scale bytes 112..141) through the small-M copy and through the one-CTA

@@ -326,10 +326,10 @@ def test_small_m_path_refuses_what_it_cannot_do():
     with pytest.raises(ops.MxStatusError) as ei:      # batched
         ops.linear(bf16_to_dev(p.x, dev), pw, path=1)
     assert ei.value.status == 2
-    big = synth.make_problem("big", 1, 65, 128, 256, seed=6)
+    big = synth.make_problem("big", 1, 129, 128, 256, seed=6)
     wq, ws = oracle_weights(big)
     pw = _pack(wq[0], ws[0], dev)
-    with pytest.raises(ops.MxStatusError):            # M > 64
+    with pytest.raises(ops.MxStatusError):            # M > 128
         ops.linear(bf16_to_dev(big.x[0], dev), pw, path=1)
     ops.check()
 

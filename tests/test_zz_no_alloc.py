@@ -58,10 +58,11 @@ def _problem(B, M, seed, x_dist="normal"):
 def _same_kernel_path(B, M):
     """The kernel the no-alloc call runs, as a forced path (restated from the
     library's rule: the small-M kernel for B = 1 and M <= 32, or M <= 64
-    where it splits K -- always at N = 512, K = 1024: 4 weight tiles, 8 K
-    tiles; else CTA pairs above 128 rows, or while one wave of pairs holds
-    every 256-column tile; else one CTA per 128 x 256 tile)."""
-    if B == 1 and M <= 64:
+    where it splits K, or M <= 128 where it splits K into ranges of at most
+    1024 -- all of these at N = 512, K = 1024: 4 weight tiles, 8 K tiles;
+    else CTA pairs above 128 rows, or while one wave of pairs holds every
+    256-column tile; else one CTA per 128 x 256 tile)."""
+    if B == 1 and M <= 128:
         return 1
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 if M > 128 or B * -(-N // 256) * 2 <= sms else 2
