@@ -139,7 +139,8 @@ def test_integer_operands_exact(fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
-@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (16, 128, 1024), (40, 256, 384)])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (16, 128, 1024), (40, 256, 384), (100, 256, 1024),
+                                   (128, 128, 512)])
 def test_small_m_path_exact(fmt, M, N, K):
     """The fused small-M kernel (weights on the MMA's A side): x = +-2^d per
     block (quantised without rounding), integer FP6 weights: exact sums."""
@@ -180,7 +181,7 @@ def test_power_of_two_scale_patterns_exact(fmt):
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("B,M,N,K,path", [(1, 1, 4096, 4096, 0), (1, 16, 4096, 1024, 0), (1, 64, 520, 512, 0),
                                           (1, 300, 520, 1024, 0), (1, 129, 264, 384, 2), (3, 200, 264, 256, 0),
-                                          (1, 4096, 1024, 512, 3)])
+                                          (1, 4096, 1024, 512, 3), (1, 128, 520, 1024, 0)])
 def test_against_oracle(fmt, B, M, N, K, path):
     """Seeded bf16 x quantised in the call, weights from bf16 N(0, 0.02)
     quantised to FP6 by the library, bias; every kernel path and a batch."""
