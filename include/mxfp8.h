@@ -227,6 +227,12 @@ mxfp8_status mxfp8_pack_scales(const uint8_t* scale, int64_t B, int64_t R, int64
  * of mxfp8_linear.  Requirements as for mxfp8_linear (N % 8 == 0, K % 128 == 0).
  *   x_q, sfa_packed : device, from mxfp8_quantize_packed (or mxfp8_pack_scales).
  *   w_packed, sf_packed : device, from mxfp8_process_weights.
+ *   With B = 1 and up to 64 rows (up to 128 where the small-M kernel's K split
+ *   leaves each CTA at most 1024 of K) the small-M kernel runs, copying the
+ *   codes and scale atoms into its operand tiles, and the output is what
+ *   mxfp8_linear gives for the x these operands were quantised from;
+ *   otherwise the large-M kernels, which here never split K (where
+ *   mxfp8_linear splits K its fp32 sums are rounded in another order).
  */
 mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
                                int64_t N, int64_t K, const uint8_t* w_packed,

@@ -421,6 +421,23 @@ mxfp8_status gemm_packed_impl(const uint8_t* x_q, const uint8_t* sfa_packed, int
   if (M == 0) return MXFP8_OK;
   int sms = 0;
   if ((st = current_device(&sms)) != MXFP8_OK) return st;
+  // Decode-sized operands (B = 1, no hand-off): the small-M kernel copies the
+  // codes and the scale bytes from their atoms, on the shapes where mxfp8_linear
+  // gives it a pre-quantised x (up to 64 rows; up to 128 where its K split
+  // leaves each CTA at most 1024 of K).
+  if (B == 1 && o.y_q == nullptr && M <= kSmallM) {
+    const int S = M > 64 ? mx::decode_k_splits(M, N, K, sms) : 0;
+    if (M <= 64 || (S >= 2 && K / S <= 1024)) {
+      mx::DecodeProblem dp{nullptr, w_packed, sf_packed, bias_bf16, o.out_bf16, M, N, K};
+      dp.xq = x_q;
+      dp.xs = sfa_packed;
+      dp.xs_packed = 1;
+      const char* msg = "";
+      cudaError_t e = mx::launch_gemm_decode(dp, sms, reinterpret_cast<cudaStream_t>(stream), &msg);
+      if (e != cudaSuccess) return cuda_fail(e, msg);
+      return MXFP8_OK;
+    }
+  }
   mx::GemmProblem p{x_q, w_packed, sfa_packed, sf_packed, bias_bf16, o.out_bf16, B, M, N, K, 0, o.y_q, o.y_sf};
   const char* msg = "";
   cudaError_t e = mx::launch_gemm_prefill(p, sms, reinterpret_cast<cudaStream_t>(stream), &msg);

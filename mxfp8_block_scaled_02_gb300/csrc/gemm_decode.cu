@@ -115,7 +115,8 @@ using WideCfg = DCfg<kDecodeMaxM, 4, 4, 2, 1>;
 struct Args {
   const uint4* x;  // bf16 [M, K] as 16-byte chunks, or nullptr:
   const uint8_t* xq;  // pre-quantised E4M3 [M, K] and
-  const uint8_t* xs;  // its row-major scales [M, K/32], copied into the slots
+  const uint8_t* xs;  // its scales [M, K/32], copied into the slots: row-major,
+  int xs_packed;      // or (1) in the packed atom layout of mxfp8_quantize_packed
   const uint8_t* sfw;
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
@@ -302,7 +303,10 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
           const uint4* src = reinterpret_cast<const uint4*>(a.xq + e0);
           dst[u][0] = valid ? __ldg(src) : make_uint4(0, 0, 0, 0);
           dst[u][1] = valid ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
-          dst[u][2].x = valid ? static_cast<uint32_t>(__ldg(a.xs + e0 / 32)) : 0u;
+          const int64_t so = a.xs_packed ? sf_packed_offset(0, rem >> 2, (kt0 + i) * 4 + (rem & 3),
+                                                            (a.M + kAtomRows - 1) / kAtomRows, a.KT)
+                                         : e0 / 32;
+          dst[u][2].x = valid ? static_cast<uint32_t>(__ldg(a.xs + so)) : 0u;
         } else {
           const uint4* src = a.x + e0 / 8;
 #pragma unroll
@@ -557,6 +561,7 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   a.x = static_cast<const uint4*>(p.x);
   a.xq = p.xq;
   a.xs = p.xs;
+  a.xs_packed = p.xs_packed;
   a.sfw = p.sfw;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.out = static_cast<__nv_bfloat16*>(p.out);

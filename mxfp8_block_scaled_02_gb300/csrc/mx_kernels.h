@@ -115,7 +115,8 @@ struct DecodeProblem {
   int64_t M, N, K;
   int wfmt = 0;      // weight element format, as GemmProblem::wfmt
   const uint8_t* xq = nullptr;  // pre-quantised x: E4M3 [M, K] ...
-  const uint8_t* xs = nullptr;  // ... and its row-major E8M0 scales [M, K/32]
+  const uint8_t* xs = nullptr;  // ... and its E8M0 scales [M, K/32]: row-major,
+  int xs_packed = 0;            // or (1) packed atoms as mxfp8_quantize_packed writes them
 };
 constexpr int kDecodeMaxM = 128;  // largest M the small-M kernel takes
 // The K split (cluster size) launch_gemm_decode uses for this shape; 1 = none.

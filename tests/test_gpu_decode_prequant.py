@@ -92,3 +92,23 @@ def test_bf16_rows_33_to_64_route(M, N, K):
     torch.cuda.synchronize()
     ops.check()
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 1032, 2048), (40, 264, 9216), (64, 520, 512),
+                                   (100, 1032, 1024), (128, 4096, 4096)])
+def test_packed_operands_match_linear(M, N, K):
+    """mxfp8_gemm_packed on mxfp8_quantize_packed(x) at decode sizes (the
+    small-M kernel reading the scale atoms) gives the bytes mxfp8_linear gives
+    on x."""
+    dev = device()
+    w = _bf16((N, K), N * 3 + K, dev, 0.05)
+    wq, ws = ops.quantize(w)
+    pw = ops.process_weights(wq, ws)
+    x = _bf16((M, K), M + 5, dev)
+    b = _bf16((N,), 9, dev, 0.1)
+    y_lin = ops.linear(x, pw, b)
+    pa = ops.quantize_packed(x)
+    y_pk = ops.gemm_packed(pa, pw, b)
+    torch.cuda.synchronize()
+    ops.check()
+    assert torch.equal(y_lin.view(torch.int16), y_pk.reshape(y_lin.shape).view(torch.int16))

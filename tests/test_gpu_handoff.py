@@ -37,10 +37,14 @@ def _unpacked_scales(pa: ops.PackedActivation) -> np.ndarray:
     return out.cpu().numpy()
 
 
-def _same_kernel(M, B, N):
-    """The unsplit large-M kernel that gemm_packed takes (restated from the
-    library's rule: CTA pairs above 128 rows, or while one wave of pairs holds
+def _same_kernel(M, B, N, hand_off=False):
+    """The kernel gemm_packed (or, with hand_off, gemm_packed_quantized_out)
+    takes, as a forced path (restated from the library's rule: without a
+    hand-off the small-M kernel for B = 1 and M <= 64; else the unsplit
+    large-M kernels: CTA pairs above 128 rows, or while one wave of pairs holds
     every 256-column tile; else one CTA per 128 x 256 tile)."""
+    if not hand_off and B == 1 and M <= 64:
+        return 1
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 if M > 128 or B * -(-N // 256) * 2 <= sms else 2
 
@@ -118,7 +122,7 @@ def test_three_layer_chain(M):
     # layer 1 as the hand-off call runs it; layers 2 and 3 as gemm_packed does
     h = x
     for i, ((pw, _, _), b) in enumerate(zip(layers, biases)):
-        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M, 1, pw.N))
+        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M, 1, pw.N, hand_off=i == 1))
     ops.check()
     assert torch.equal(out3.view(torch.int16), h.view(torch.int16)), "hand-off chain differs from bf16 chain"
 
