@@ -110,14 +110,20 @@ struct PArgs {
   int splits;       // K splits per tile (split-K): > 1 writes fp32 partials through tmPart
   int units;        // total_tiles * splits
   int sfa_rowmajor; // 1: sfa is the caller's row-major x_scale (no repack kernel before this one)
+  int n_fast;       // tile order: 1 = column tiles vary fastest, 0 = row tiles
 };
 
 __device__ __forceinline__ void pair_tile_coords(int tile, const PArgs& a, int& b, int& mt2, int& nt) {
   const int per_b = a.MT2 * a.NT;
   b = tile / per_b;
   const int t = tile - b * per_b;
-  nt = t / a.MT2;
-  mt2 = t - nt * a.MT2;
+  if (a.n_fast) {
+    mt2 = t / a.NT;
+    nt = t - mt2 * a.NT;
+  } else {
+    nt = t / a.MT2;
+    mt2 = t - nt * a.MT2;
+  }
 }
 
 // Work unit u = tile * splits + s: output tile `tile`, K tiles [kt_lo, kt_hi)
@@ -689,6 +695,10 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   a.total_tiles = a.B * a.MT2 * a.NT;
   a.splits = splits;
   a.units = a.total_tiles * splits;
+  // The pairs of one round run consecutive tiles at once: sweep the operand
+  // with fewer bytes fastest, so that it stays in L2 while each tile of the
+  // larger one is read from DRAM once (M > N: the weights stay resident).
+  a.n_fast = p.M > p.N ? 1 : 0;
   // split-K: the partials carry no bias and no hand-off; the reduce adds them
   if (splits > 1) {
     a.bias = nullptr;
