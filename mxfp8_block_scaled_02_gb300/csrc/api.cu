@@ -302,7 +302,9 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
 
   // The small-M kernel (every threshold below measured in CUDA graphs of
   // back-to-back calls):
-  //  * has no quantised-output epilogue: the hand-off takes the large-M kernels;
+  //  * quantises its output for the hand-off only where it splits K at most
+  //    four ways (a warp then holds each 32-column block); with an 8-way
+  //    split the hand-off takes the large-M kernels;
   //  * up to 32 rows, quantises bf16 x inside every CTA;
   //  * from 33 to 64 rows of bf16 x, does so only while each CTA's K range is
   //    short (K split, K / S <= 1024: N = K = 4096, M = 48 / 64 9.0 / 9.5 us);
@@ -325,10 +327,11 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   const bool short_k = dec_splits >= 2 && K / dec_splits <= 1024;  // each CTA's K range
   const bool wide_ok = M > 64 && M <= kSmallM && short_k;
   const WsLayout qws = prefill_workspace(1, M, N, K, false, 1);
-  const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && o.y_q == nullptr &&
+  const bool hand_ok = o.y_q == nullptr || (B == 1 && M <= kSmallM && mx::decode_k_splits(M, N, K, sms) <= 4);
+  const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && hand_ok &&
                           ((M <= 64 && !short_k) || wide_ok) && workspace != nullptr && aligned(workspace, 256) &&
                           static_cast<int64_t>(workspace_bytes) >= qws.total;
-  const bool small_ok = B == 1 && M <= kSmallM && o.y_q == nullptr &&
+  const bool small_ok = B == 1 && M <= kSmallM && hand_ok &&
                         (path == 1 || M <= 32 || (M <= 64 && (have_q || copy_route || dec_splits >= 2)) || wide_ok);
   if (path == 1 && !small_ok)
     return fail(MXFP8_ERR_UNSUPPORTED, "the small-M path needs B == 1, M <= %d and no quantised output", kSmallM);
@@ -336,6 +339,8 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
     mx::DecodeProblem p{x_bf16, w_packed, sf_packed, bias_bf16, out_bf16, M, N, K, w_format};
     p.xq = x_q;
     p.xs = x_scale;
+    p.yq = o.y_q;
+    p.ysf = o.y_sf;
     if (copy_route) {
       uint8_t* wsb = static_cast<uint8_t*>(workspace);
       cudaError_t e = mx::launch_quantize(x_bf16, M, K, wsb + qws.xq_off, wsb + qws.sfa_off, false, 1, M, sms, s,
@@ -421,17 +426,20 @@ mxfp8_status gemm_packed_impl(const uint8_t* x_q, const uint8_t* sfa_packed, int
   if (M == 0) return MXFP8_OK;
   int sms = 0;
   if ((st = current_device(&sms)) != MXFP8_OK) return st;
-  // Decode-sized operands (B = 1, no hand-off): the small-M kernel copies the
-  // codes and the scale bytes from their atoms, on the shapes where mxfp8_linear
-  // gives it a pre-quantised x (up to 64 rows; up to 128 where its K split
-  // leaves each CTA at most 1024 of K).
-  if (B == 1 && o.y_q == nullptr && M <= kSmallM) {
-    const int S = M > 64 ? mx::decode_k_splits(M, N, K, sms) : 0;
-    if (M <= 64 || (S >= 2 && K / S <= 1024)) {
+  // Decode-sized operands (B = 1): the small-M kernel copies the codes and
+  // the scale bytes from their atoms, on the shapes where mxfp8_linear gives
+  // it a pre-quantised x (up to 64 rows; up to 128 where its K split leaves
+  // each CTA at most 1024 of K), with a hand-off only where it splits K at
+  // most four ways, as mxfp8_linear_quantized_out.
+  if (B == 1 && M <= kSmallM) {
+    const int S = mx::decode_k_splits(M, N, K, sms);
+    if ((o.y_q == nullptr || S <= 4) && (M <= 64 || (S >= 2 && K / S <= 1024))) {
       mx::DecodeProblem dp{nullptr, w_packed, sf_packed, bias_bf16, o.out_bf16, M, N, K};
       dp.xq = x_q;
       dp.xs = sfa_packed;
       dp.xs_packed = 1;
+      dp.yq = o.y_q;
+      dp.ysf = o.y_sf;
       const char* msg = "";
       cudaError_t e = mx::launch_gemm_decode(dp, sms, reinterpret_cast<cudaStream_t>(stream), &msg);
       if (e != cudaSuccess) return cuda_fail(e, msg);

@@ -126,12 +126,18 @@ struct Args {
   int RTW;     // 128-row atom tiles of the weights
   int splits;  // cluster size S
   int wfmt;    // weight (A operand) element format
+  uint8_t* yq;   // MXFP8 hand-off of the output (kHandOff): E4M3 [M, N] ...
+  uint8_t* ysf;  // ... and its scales in packed atoms (one 128-row tile)
+  int KTY;       // N / 128: K tiles of the hand-off's scale atoms
 };
 
 // kPreQ: x arrives pre-quantised (a.xq, a.xs) and is copied, not quantised;
 // a separate instantiation, so that the bf16 path carries no branch for it
 // (a run-time test cost that path ~0.25 us per call at N = K = 4096).
-template <class C, bool kPreQ>
+// kHandOff: the output is also quantised for the next layer (a.yq, a.ysf;
+// a.out may then be null): needs N % 128 == 0 and a K split of at most 4, so
+// that one warp holds the 32 columns of each block.
+template <class C, bool kPreQ, bool kHandOff>
 __global__ void __launch_bounds__(THREADS, C::MINB)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -377,8 +383,19 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float v = nk > 1 ? __uint_as_float(r[j]) + __uint_as_float(r1[j]) : __uint_as_float(r[j]);
-          if (c + j < a.M && n < a.N)
-            a.out[static_cast<int64_t>(c + j) * a.N + n] = __float2bfloat16_rn((0.f + v) + bias_n);
+          if constexpr (kHandOff) {
+            if (c + j < a.M) {  // the same row in every lane: the warp is one block
+              const __nv_bfloat16 yb = __float2bfloat16_rn((0.f + v) + bias_n);
+              if (a.out != nullptr) a.out[static_cast<int64_t>(c + j) * a.N + n] = yb;
+              uint32_t sb;
+              const uint32_t code = quantize_lane_block(__bfloat16_as_ushort(yb), &sb);
+              a.yq[static_cast<int64_t>(c + j) * a.N + n] = static_cast<uint8_t>(code);
+              if (lane == 0) a.ysf[sf_packed_offset(0, c + j, n >> 5, 1, a.KTY)] = static_cast<uint8_t>(sb);
+            }
+          } else {
+            if (c + j < a.M && n < a.N)
+              a.out[static_cast<int64_t>(c + j) * a.N + n] = __float2bfloat16_rn((0.f + v) + bias_n);
+          }
         }
       }
     }
@@ -423,7 +440,17 @@ __global__ void __launch_bounds__(THREADS, C::MINB)
       for (int m = t / per; m < a.M; m += QTHREADS / per) {
         float acc = 0.f;
         for (int s2 = 0; s2 < a.splits; ++s2) acc += recv[(s2 * a.n_mma + m) * per + nl];
-        a.out[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc + bias);
+        if constexpr (kHandOff) {
+          // per >= 32: the warp holds one 32-column block of row m
+          const __nv_bfloat16 yb = __float2bfloat16_rn(acc + bias);
+          if (a.out != nullptr) a.out[static_cast<int64_t>(m) * a.N + n] = yb;
+          uint32_t sb;
+          const uint32_t code = quantize_lane_block(__bfloat16_as_ushort(yb), &sb);
+          a.yq[static_cast<int64_t>(m) * a.N + n] = static_cast<uint8_t>(code);
+          if (lane == 0) a.ysf[sf_packed_offset(0, m, n >> 5, 1, a.KTY)] = static_cast<uint8_t>(sb);
+        } else {
+          a.out[static_cast<int64_t>(m) * a.N + n] = __float2bfloat16_rn(acc + bias);
+        }
       }
     }
   }
@@ -440,11 +467,12 @@ cudaError_t prepare_cfg(const char** msg) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<C, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_decode_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM_ALLOC);
+    void (*const kernels[4])(const CUtensorMap, const Args) = {
+        gemm_decode_kernel<C, false, false>, gemm_decode_kernel<C, true, false>, gemm_decode_kernel<C, false, true>,
+        gemm_decode_kernel<C, true, true>};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) {
       *msg = "cudaFuncSetAttribute(max dynamic shared memory) failed";
       return e;
@@ -476,7 +504,7 @@ int max_active_clusters(int splits) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<C, false>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<C, false, false>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();  // clear the sticky-free error state of the failed query
       n = -1;
     }
@@ -485,7 +513,7 @@ int max_active_clusters(int splits) {
   return cache[dev][slot];
 }
 
-template <class C, bool kPreQ>
+template <class C, bool kPreQ, bool kHandOff>
 cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStream_t stream,
                        const char** msg) {
   cudaLaunchConfig_t cfg = {};
@@ -502,7 +530,7 @@ cudaError_t launch_cfg(const CUtensorMap& mw, const Args& a, int grid, cudaStrea
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<C, kPreQ>, mw, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<C, kPreQ, kHandOff>, mw, a);
   if (e != cudaSuccess) *msg = "decode GEMM launch failed";
   return e;
 }
@@ -547,7 +575,16 @@ cudaError_t launch_with(const CUtensorMap& mw, Args& a, bool preq, int sms, cuda
   if (e != cudaSuccess) return e;
   a.splits = k_splits<C>(a.RTW, a.KT, sms);
   const int grid = a.RTW * a.splits;
-  return preq ? launch_cfg<C, true>(mw, a, grid, stream, msg) : launch_cfg<C, false>(mw, a, grid, stream, msg);
+  if (a.yq != nullptr) {
+    if (a.splits > 4 || a.N % 128 != 0) {
+      *msg = "small-M hand-off: needs N % 128 == 0 and a K split of at most 4";
+      return cudaErrorInvalidValue;
+    }
+    return preq ? launch_cfg<C, true, true>(mw, a, grid, stream, msg)
+                : launch_cfg<C, false, true>(mw, a, grid, stream, msg);
+  }
+  return preq ? launch_cfg<C, true, false>(mw, a, grid, stream, msg)
+              : launch_cfg<C, false, false>(mw, a, grid, stream, msg);
 }
 
 }  // namespace
@@ -562,6 +599,9 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   a.xq = p.xq;
   a.xs = p.xs;
   a.xs_packed = p.xs_packed;
+  a.yq = p.yq;
+  a.ysf = p.ysf;
+  a.KTY = static_cast<int>(p.N / 128);
   a.sfw = p.sfw;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.out = static_cast<__nv_bfloat16*>(p.out);

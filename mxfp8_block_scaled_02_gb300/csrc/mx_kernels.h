@@ -117,6 +117,8 @@ struct DecodeProblem {
   const uint8_t* xq = nullptr;  // pre-quantised x: E4M3 [M, K] ...
   const uint8_t* xs = nullptr;  // ... and its E8M0 scales [M, K/32]: row-major,
   int xs_packed = 0;            // or (1) packed atoms as mxfp8_quantize_packed writes them
+  uint8_t* yq = nullptr;        // MXFP8 hand-off of the output (E4M3 [M, N]) and its
+  uint8_t* ysf = nullptr;       // packed scales; out may then be null (N % 128 == 0, K split <= 4)
 };
 constexpr int kDecodeMaxM = 128;  // largest M the small-M kernel takes
 // The K split (cluster size) launch_gemm_decode uses for this shape; 1 = none.

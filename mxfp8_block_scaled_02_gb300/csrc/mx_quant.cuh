@@ -54,6 +54,21 @@ __device__ __forceinline__ uint32_t quantize_quarter_block(const uint4 v, uint2&
   return sbyte;
 }
 
+// One bf16 value per lane, the 32 lanes of the warp one 32-element block (lane
+// i = element i): the same decisions as quantize_block32 on the same bits.
+// Must be called by all 32 lanes.  Returns this lane's E4M3 code; the block's
+// scale byte goes to *sbyte (the same in every lane).
+__device__ __forceinline__ uint32_t quantize_lane_block(uint32_t bf16_bits, uint32_t* sbyte) {
+  const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, bf16_bits & 0x7FFFu);
+  const bool nonfinite = amax >= 0x7F80u;
+  const uint32_t E = amax >> 7;
+  const uint32_t sb = nonfinite ? 0xFFu : (E > 8u ? E - 8u : 0u);
+  const float mul = __uint_as_float((254u - (nonfinite ? 0u : sb)) << 23);
+  const uint32_t code = cvt_e4m3x2(__uint_as_float(bf16_bits << 16) * mul, 0.f) & 0xFFu;
+  *sbyte = sb;
+  return nonfinite ? 0x7Fu : code;
+}
+
 // Element formats of a quantised block: kFmtE4M3 for activations and MXFP8
 // weights; kFmtE2M3 / kFmtE3M2 for MXFP6 weights (the mxfp6 page's
 // kMxfp6E2M3Static / kMxfp6E3M2Static), one 6-bit code per byte here.

@@ -37,27 +37,33 @@ def _unpacked_scales(pa: ops.PackedActivation) -> np.ndarray:
     return out.cpu().numpy()
 
 
-def _same_kernel(M, B, N, hand_off=False):
-    """The kernel gemm_packed (or, with hand_off, gemm_packed_quantized_out)
-    takes, as a forced path (restated from the library's rule: without a
-    hand-off the small-M kernel for B = 1 and M <= 64; else the unsplit
-    large-M kernels: CTA pairs above 128 rows, or while one wave of pairs holds
-    every 256-column tile; else one CTA per 128 x 256 tile)."""
-    if not hand_off and B == 1 and M <= 64:
+def _same_kernel(M, B, N):
+    """The kernel gemm_packed and gemm_packed_quantized_out take at these test
+    shapes (K <= 512), as a forced path (restated from the library's rule: the
+    small-M kernel for B = 1 and M <= 64 -- its K split is at most K / 128 <= 4,
+    so the hand-off may use it too; else the unsplit large-M kernels: CTA
+    pairs above 128 rows, or while one wave of pairs holds every 256-column
+    tile; else one CTA per 128 x 256 tile)."""
+    if B == 1 and M <= 64:
         return 1
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 if M > 128 or B * -(-N // 256) * 2 <= sms else 2
 
 
-# the path whose kernels the hand-off of a linear call uses (large-M kernels,
-# split-K included), so its bf16 output must match this path bit for bit
+# the large-M kernels, split-K included: what the hand-off of a linear call
+# runs beyond decode sizes, so its bf16 output must match this path bit for bit
 HAND_OFF_PATH = 4
 
 
-@pytest.mark.parametrize("B,M,N,K,bias", [(1, 300, 512, 1024, True), (1, 64, 256, 512, False),
-                                          (1, 1, 128, 256, True), (2, 200, 384, 256, True),
-                                          (1, 520, 1024, 384, False)])
-def test_hand_off_bytes_equal_the_oracle_quantiser(B, M, N, K, bias):
+# ref_path: the kernels whose bf16 output the hand-off's must equal -- mxfp8_linear's
+# own choice (0), or the large-M kernels (4) where its small-M kernel would
+# split K eight ways (8 weight tiles, 16 K tiles: 8 clusters of 8 fit)
+@pytest.mark.parametrize("B,M,N,K,bias,ref_path", [(1, 300, 512, 1024, True, 0), (1, 64, 256, 512, False, 0),
+                                                   (1, 1, 128, 256, True, 0), (2, 200, 384, 256, True, 0),
+                                                   (1, 520, 1024, 384, False, 0), (1, 1, 4096, 4096, True, 0),
+                                                   (1, 16, 14336, 4096, True, 0), (1, 100, 4096, 4096, False, 0),
+                                                   (1, 16, 1024, 2048, True, 4)])
+def test_hand_off_bytes_equal_the_oracle_quantiser(B, M, N, K, bias, ref_path):
     dev = device()
     p = synth.make_problem("handoff", B, M, N, K, seed=B * 100 + M + N, bias_std=0.1 if bias else None,
                            x_dist="laplace")
@@ -65,7 +71,7 @@ def test_hand_off_bytes_equal_the_oracle_quantiser(B, M, N, K, bias):
     x = bf16_to_dev(p.x if B > 1 else p.x[0], dev)
     b = None if p.bias is None else bf16_to_dev(p.bias, dev)
     out, y = ops.linear_quantized_out(x, pw, b)
-    ref = ops.linear(x, pw, b, path=HAND_OFF_PATH)
+    ref = ops.linear(x, pw, b, path=ref_path)
     ops.check()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), "bf16 output differs from mxfp8_linear"
 
@@ -119,10 +125,11 @@ def test_three_layer_chain(M):
     out3 = ops.gemm_packed(y2, layers[2][0], biases[2])[0]
     ops.check()
 
-    # layer 1 as the hand-off call runs it; layers 2 and 3 as gemm_packed does
+    # layer 1 as the hand-off call runs it (mxfp8_linear's choice); layers 2 and 3
+    # as gemm_packed and gemm_packed_quantized_out do
     h = x
     for i, ((pw, _, _), b) in enumerate(zip(layers, biases)):
-        h = ops.linear(h, pw, b, path=HAND_OFF_PATH if i == 0 else _same_kernel(M, 1, pw.N, hand_off=i == 1))
+        h = ops.linear(h, pw, b, path=0 if i == 0 else _same_kernel(M, 1, pw.N))
     ops.check()
     assert torch.equal(out3.view(torch.int16), h.view(torch.int16)), "hand-off chain differs from bf16 chain"
 
