@@ -251,9 +251,9 @@ mxfp8_status mxfp8_gemm_packed(const uint8_t* x_q, const uint8_t* sfa_packed, in
  *   (padding rows of the last atom tile are left as they were).  The call
  *   runs the kernels mxfp8_linear chooses and y is its output bit for bit,
  *   except at B = 1 and decode sizes where mxfp8_linear's small-M kernel
- *   would split K eight ways (N below ~2048): the hand-off then runs on the
- *   large-M kernels (mxfp8_linear_path path 4), whose fp32 sums are rounded
- *   in another order.
+ *   splits K eight ways (N below ~2048): the hand-off splits it four ways
+ *   (whole 32-column blocks per CTA), so its fp32 sums are rounded in
+ *   another order.
  *   Inputs, w_packed, sf_packed, bias, workspace: as mxfp8_linear (either x
  *   form; the workspace of mxfp8_workspace_size).
  *   out_bf16    : device, [B, M, N] bf16 out, or NULL to skip the bf16 output.
@@ -276,8 +276,8 @@ mxfp8_status mxfp8_linear_quantized_out(const void* x_bf16, const uint8_t* x_q, 
  * hand-off output as mxfp8_linear_quantized_out: the step of a chain of layers
  * whose input is the previous layer's y_q / y_sf_packed and whose output feeds
  * the next.  Source and arguments as those two calls (out_bf16 may be NULL;
- * N % 128 == 0); the kernel choice as mxfp8_gemm_packed's, with the hand-off
- * on the small-M kernel only where it splits K at most four ways.
+ * N % 128 == 0); the kernel choice as mxfp8_gemm_packed's, K split at most
+ * four ways on the small-M kernel.
  */
 mxfp8_status mxfp8_gemm_packed_quantized_out(const uint8_t* x_q, const uint8_t* sfa_packed, int64_t B, int64_t M,
                                              int64_t N, int64_t K, const uint8_t* w_packed,

@@ -302,9 +302,9 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
 
   // The small-M kernel (every threshold below measured in CUDA graphs of
   // back-to-back calls):
-  //  * quantises its output for the hand-off only where it splits K at most
-  //    four ways (a warp then holds each 32-column block); with an 8-way
-  //    split the hand-off takes the large-M kernels;
+  //  * quantises its output for the hand-off with K split at most four ways
+  //    (a warp then holds each 32-column block; where it would split eight
+  //    ways the hand-off splits four, so its sums round in another order);
   //  * up to 32 rows, quantises bf16 x inside every CTA;
   //  * from 33 to 64 rows of bf16 x, does so only while each CTA's K range is
   //    short (K split, K / S <= 1024: N = K = 4096, M = 48 / 64 9.0 / 9.5 us);
@@ -327,7 +327,7 @@ mxfp8_status linear_impl(int path, const void* x_bf16, const uint8_t* x_q, const
   const bool short_k = dec_splits >= 2 && K / dec_splits <= 1024;  // each CTA's K range
   const bool wide_ok = M > 64 && M <= kSmallM && short_k;
   const WsLayout qws = prefill_workspace(1, M, N, K, false, 1);
-  const bool hand_ok = o.y_q == nullptr || (B == 1 && M <= kSmallM && mx::decode_k_splits(M, N, K, sms) <= 4);
+  const bool hand_ok = o.y_q == nullptr || (B == 1 && M <= kSmallM);
   const bool copy_route = path == 0 && have_x && B == 1 && M > 32 && hand_ok &&
                           ((M <= 64 && !short_k) || wide_ok) && workspace != nullptr && aligned(workspace, 256) &&
                           static_cast<int64_t>(workspace_bytes) >= qws.total;
@@ -429,11 +429,10 @@ mxfp8_status gemm_packed_impl(const uint8_t* x_q, const uint8_t* sfa_packed, int
   // Decode-sized operands (B = 1): the small-M kernel copies the codes and
   // the scale bytes from their atoms, on the shapes where mxfp8_linear gives
   // it a pre-quantised x (up to 64 rows; up to 128 where its K split leaves
-  // each CTA at most 1024 of K), with a hand-off only where it splits K at
-  // most four ways, as mxfp8_linear_quantized_out.
+  // each CTA at most 1024 of K); a hand-off as in mxfp8_linear_quantized_out.
   if (B == 1 && M <= kSmallM) {
-    const int S = mx::decode_k_splits(M, N, K, sms);
-    if ((o.y_q == nullptr || S <= 4) && (M <= 64 || (S >= 2 && K / S <= 1024))) {
+    const int S = M > 64 ? mx::decode_k_splits(M, N, K, sms) : 0;
+    if (M <= 64 || (S >= 2 && K / S <= 1024)) {
       mx::DecodeProblem dp{nullptr, w_packed, sf_packed, bias_bf16, o.out_bf16, M, N, K};
       dp.xq = x_q;
       dp.xs = sfa_packed;

@@ -135,8 +135,8 @@ struct Args {
 // a separate instantiation, so that the bf16 path carries no branch for it
 // (a run-time test cost that path ~0.25 us per call at N = K = 4096).
 // kHandOff: the output is also quantised for the next layer (a.yq, a.ysf;
-// a.out may then be null): needs N % 128 == 0 and a K split of at most 4, so
-// that one warp holds the 32 columns of each block.
+// a.out may then be null): needs N % 128 == 0, and the launcher splits K at
+// most 4 ways, so that one warp holds the 32 columns of each block.
 template <class C, bool kPreQ, bool kHandOff>
 __global__ void __launch_bounds__(THREADS, C::MINB)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const Args a) {
@@ -574,15 +574,17 @@ cudaError_t launch_with(const CUtensorMap& mw, Args& a, bool preq, int sms, cuda
   cudaError_t e = prepare_cfg<C>(msg);
   if (e != cudaSuccess) return e;
   a.splits = k_splits<C>(a.RTW, a.KT, sms);
-  const int grid = a.RTW * a.splits;
   if (a.yq != nullptr) {
-    if (a.splits > 4 || a.N % 128 != 0) {
-      *msg = "small-M hand-off: needs N % 128 == 0 and a K split of at most 4";
+    // the hand-off needs whole 32-column blocks in one owner: at most 4 ways
+    if (a.N % 128 != 0) {
+      *msg = "small-M hand-off: needs N % 128 == 0";
       return cudaErrorInvalidValue;
     }
-    return preq ? launch_cfg<C, true, true>(mw, a, grid, stream, msg)
-                : launch_cfg<C, false, true>(mw, a, grid, stream, msg);
+    if (a.splits > 4) a.splits = 4;
+    return preq ? launch_cfg<C, true, true>(mw, a, a.RTW * a.splits, stream, msg)
+                : launch_cfg<C, false, true>(mw, a, a.RTW * a.splits, stream, msg);
   }
+  const int grid = a.RTW * a.splits;
   return preq ? launch_cfg<C, true, false>(mw, a, grid, stream, msg)
               : launch_cfg<C, false, false>(mw, a, grid, stream, msg);
 }
