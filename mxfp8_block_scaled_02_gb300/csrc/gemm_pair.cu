@@ -697,8 +697,10 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int sms, cudaStream_t stream,
   a.units = a.total_tiles * splits;
   // The pairs of one round run consecutive tiles at once: sweep the operand
   // with fewer bytes fastest, so that it stays in L2 while each tile of the
-  // larger one is read from DRAM once (M > N: the weights stay resident).
-  a.n_fast = p.M > p.N ? 1 : 0;
+  // larger one is read from DRAM once (M >= N: the weights stay resident;
+  // at M = N, K = 14336 behind a hand-off this measured 347.5 -> 342.7 us
+  // for the two-layer chain).
+  a.n_fast = p.M >= p.N ? 1 : 0;
   // split-K: the partials carry no bias and no hand-off; the reduce adds them
   if (splits > 1) {
     a.bias = nullptr;
