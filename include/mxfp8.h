@@ -153,7 +153,9 @@ mxfp8_status mxfp8_workspace_size(int64_t B, int64_t M, int64_t N, int64_t K,
  *   serialization.  When the kernel before them in the stream triggers its
  *   dependents early (griddepcontrol.launch_dependents), they may read
  *   w_packed, sf_packed and bias before that kernel ends; x, x_q, x_scale
- *   and out are touched only after it has finished.  Of this library's
+ *   and out are touched only after it has finished.  The quantise step inside
+ *   a linear call is launched the same way and touches nothing before the
+ *   kernel ahead of it has finished.  Of this library's
  *   kernels, only these trigger early: the quantise / activation-scale repack
  *   step inside mxfp8_linear, mxfp8_linear_path and mxfp8_linear_noalloc
  *   (whose output only the same call's GEMM reads, after its wait), the
