@@ -107,6 +107,11 @@ struct DCfg {
 // measured 8.45 us per call at M = 1 against 9.10 us for a 4-stage ring at two
 // CTAs per SM, whose second half of the slice refilled on the critical path.
 using SmallCfg = DCfg<16, 8, 8, 1, 1>;
+// Up to 16 tokens where a CTA's K slice is longer than 8 tiles (no split at
+// large N): an 11-stage weight ring, the most that fits beside the 8-slot
+// activation ring (N = 14336, K = 4096: 14.2 -> 13.4 us at M = 1; at
+// N = K = 4096 it measured 6.02 -> 6.12 us, so the 8-stage shape stays there).
+using DeepCfg = DCfg<16, 11, 8, 1, 1>;
 using LargeCfg = DCfg<64, 6, 8, 2, 1>;
 // Up to 128 tokens (a prefill chunk): 4-slot rings of 16 KB weight tiles and
 // 16 KB code tiles, a 64 KB receive buffer, two 128-column accumulators.
@@ -616,7 +621,14 @@ cudaError_t launch_gemm_decode(const DecodeProblem& p, int sms, cudaStream_t str
   a.KT = static_cast<int>(p.K / kTK);
   a.RTW = static_cast<int>(ceil_div(p.N, kAtomRows));
   const bool preq = p.xq != nullptr;
-  if (a.n_mma <= SmallCfg::MAXTOK) return launch_with<SmallCfg>(mw, a, preq, sms, stream, msg);
+  if (a.n_mma <= SmallCfg::MAXTOK) {
+    // the same split either way (one CTA per SM, the same cluster sizes)
+    e = prepare_cfg<SmallCfg>(msg);
+    if (e != cudaSuccess) return e;
+    if (a.KT / k_splits<SmallCfg>(a.RTW, a.KT, sms) > SmallCfg::STAGES)
+      return launch_with<DeepCfg>(mw, a, preq, sms, stream, msg);
+    return launch_with<SmallCfg>(mw, a, preq, sms, stream, msg);
+  }
   if (a.n_mma <= LargeCfg::MAXTOK) return launch_with<LargeCfg>(mw, a, preq, sms, stream, msg);
   return launch_with<WideCfg>(mw, a, preq, sms, stream, msg);
 }

@@ -131,6 +131,7 @@ LINEAR_CASES = [
     (2, 100, 264, 4096, 4, "e4m3", True),
     (1, 300, 4096, 8192, 0, "e4m3", False),  # 32 tiles split two ways (long K)
     (4, 300, 136, 256, 5, "e4m3", False),    # x quantised inside the GEMM
+    (1, 5, 10240, 2048, 1, "e4m3", False),   # ... its deep-ring shape (16 K tiles per CTA, no split)
     (1, 5, 264, 512, 1, "e4m3", True),       # small-M kernel copying a pre-quantised x
     (1, 40, 520, 1024, 0, "e4m3", True),
     (1, 40, 264, 9216, 0, "e4m3", False),    # ... x quantised once into the workspace, then copied
