@@ -135,6 +135,8 @@ LINEAR_CASES = [
     (1, 5, 264, 512, 1, "e4m3", True),       # small-M kernel copying a pre-quantised x
     (1, 40, 520, 1024, 0, "e4m3", True),
     (1, 40, 264, 9216, 0, "e4m3", False),    # ... x quantised once into the workspace, then copied
+    (1, 100, 1032, 1024, 0, "e4m3", False),  # the 128-token shape (x quantised once, copied) ...
+    (1, 100, 1032, 1024, 0, "e4m3", True),   # ... and on a pre-quantised x
     (1, 5, 264, 512, 1, "e3m2", False),      # MXFP6 weights on each kind of kernel
     (1, 130, 264, 512, 3, "e2m3", False),
     (2, 256, 264, 512, 5, "e2m3", False),
