@@ -36,7 +36,10 @@ def test_two_streams_match_sequential_calls():
              _case(300, 1024, 2048, 2, dev),        # CTA pairs
              _case(256, 2048, 4096, 3, dev),        # split-K + reduce
              _case(40, 512, 1024, 4, dev, "e2m3"),  # small-M, MXFP6 weights
-             _case(700, 512, 512, 5, dev)]          # CTA pairs, two row tiles
+             _case(700, 512, 512, 5, dev),          # CTA pairs, two row tiles
+             _case(100, 1032, 1024, 6, dev),        # 128-token small-M shape, x quantised once into the workspace
+             _case(40, 264, 9216, 7, dev),          # 64-token shape on codes quantised once
+             _case(16, 1024, 4096, 8, dev)]         # small-M; its hand-off splits K four ways instead of eight
 
     def run_all():
         outs = []
