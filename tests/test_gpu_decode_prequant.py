@@ -112,3 +112,25 @@ def test_packed_operands_match_linear(M, N, K):
     torch.cuda.synchronize()
     ops.check()
     assert torch.equal(y_lin.view(torch.int16), y_pk.reshape(y_lin.shape).view(torch.int16))
+
+
+def test_copy_route_without_workspace_gives_the_same_bytes():
+    """Rows 33..64 of bf16 x on a long K range quantise x once into the
+    workspace; given no workspace, the C ABI runs the small-M kernel's own
+    quantiser instead: the same bytes."""
+    dev = device()
+    M, N, K = 40, 264, 9216
+    w = _bf16((N, K), 3, dev, 0.05)
+    wq, ws = ops.quantize(w)
+    pw = ops.process_weights(wq, ws)
+    x = _bf16((M, K), 4, dev)
+    b = _bf16((N,), 5, dev, 0.1)
+    ref = ops.linear(x, pw, b)                       # with the documented workspace
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    st = ops.load().mxfp8_linear(x.data_ptr(), None, None, 1, M, N, K, pw.w_packed.data_ptr(),
+                                 pw.sf_packed.data_ptr(), b.data_ptr(), out.data_ptr(), None, 0,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == 0, ops.load().mxfp8_last_error().decode()
+    torch.cuda.synchronize()
+    ops.check()
+    assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
